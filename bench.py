@@ -1,0 +1,481 @@
+"""Benchmark of the paged decode / step attention path on one or more GPUs.
+
+Default workload: one Mistral-7B-v0.3-shaped layer decode step (64 rows,
+32 q / 8 kv heads, head_dim 128, context lengths uniform in [512, 8192],
+pages of 64 shuffled in a pool sized to the total, bf16 synthetic data).
+A step is one pass of the whole path: append_rope over the step's tokens,
+then decode_attn (or step_attn for the Llama step workload).
+
+Metric: achieved HBM GB/s = algorithmic bytes of a step (the visible K/V
+bytes, each page counted once, plus q in, q/k/v append traffic, outputs and
+page-table entries) / step time; row-steps/s alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lnk|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own batch of
+rows (weak scaling: rows are independent, no exchange in the path); the
+timed region is bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIGS = {
+    "mistral": "Mistral-7B-v0.3-shaped layer, 64 decode rows, lengths U[512,8192]",
+    "phi3_tiny": "Phi-3-mini-shaped tiny layer, 4 rows, MHA 32/32, head_dim 96",
+    "phi3_window": "Phi-3-mini sliding-window layer, 32 rows, window 2047",
+    "qwen3": "Qwen3-4B-shaped layer, 256 rows, QK-norm, shared prefix pages",
+    "llama_step": "Llama-3.1-8B-shaped step_paged layer, 4x512 chunk tokens + 128 decode rows",
+}
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and row-steps/sec per layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes a step must move at least once, by part."""
+    d, hq, hkv = w.head_dim, w.hq, w.hkv
+    # decode rows: visible K/V keys, a page shared by several rows counted once
+    # (the covered in-page range of a shared page is the union of the rows' ranges)
+    cover = {}
+    table_entries = 0
+    for b, p in enumerate(w.dec_positions):
+        p = int(p)
+        if p < 0:
+            continue
+        lo = max(0, p - w.window + 1) if w.window else 0
+        lps = np.arange(lo // 64, p // 64 + 1)
+        table_entries += len(lps)
+        a = np.maximum(lo, lps * 64) - lps * 64
+        z = np.minimum(p, lps * 64 + 63) - lps * 64
+        for pg, aa, zz in zip(w.table[b, lps].tolist(), a.tolist(), z.tolist()):
+            if pg in cover:
+                c = cover[pg]
+                cover[pg] = (min(c[0], aa), max(c[1], zz))
+            else:
+                cover[pg] = (aa, zz)
+    kv_keys = sum(z - a + 1 for a, z in cover.values())
+    dec_kv = 2 * hkv * kv_keys * d * 2
+    dec_q_out = 2 * w.B * hq * d * 2                     # q read + out written
+    dec_table = 4 * table_entries
+    # chunk tokens: their rows' visible keys (each key once per row)
+    ch_kv = 0
+    if w.P:
+        per_row = {}
+        for r, p in zip(w.ch_rows, w.ch_positions):
+            lo = max(0, int(p) - w.window + 1) if w.window else 0
+            a, z = per_row.get(int(r), (lo, int(p)))
+            per_row[int(r)] = (min(a, lo), max(z, int(p)))
+        ch_kv = sum(2 * hkv * (z - a + 1) * d * 2 for a, z in per_row.values())
+    ch_q_out = 2 * w.P * hq * d * 2
+    append = w.T * (hq + 2 * hkv) * d * 2 + w.T * (hq + 2 * hkv) * d * 2 + 8 * w.T
+    return {"decode_kv": dec_kv, "decode_q_out": dec_q_out, "decode_table": dec_table,
+            "chunk_kv": ch_kv, "chunk_q_out": ch_q_out, "append": append,
+            "decode_call": dec_kv + dec_q_out + dec_table,
+            "step": dec_kv + dec_q_out + dec_table + ch_kv + ch_q_out + append}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_file: str, config: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "paged_kv_gqa_row_gb300", "csrc", kernel_file), "rb").read()
+        entry = rec.get(config)
+        if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return float(entry["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t_on is not None and self.t_on - 0.06 <= t <= (self.t_off or t) + 0.06]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, rows, repeats=1):
+    """Time the oracle (as it stands) on a sample of decode rows; returns
+    (seconds, algorithmic bytes of the sample, threads)."""
+    import synth  # noqa: F401
+    from oracle import paged, rope
+    sample = []
+    tp, tr = w.token_positions(), w.token_rows()
+    inv = rope.inv_freq(w.theta, w.head_dim, w.llama3)
+    q_all, k_all, v_all = w.step_q(), w.step_k(), w.step_v()
+    gq, gk = w.gamma_q(), w.gamma_k()
+    for b in rows:
+        t = w.P + b
+        p = int(tp[t])
+        lo = max(0, p - w.window + 1) if w.window else 0
+        lps = np.arange(lo // 64, p // 64 + 1)
+        pages = w.table[b, lps]
+        kp = np.stack([w.pool_pages("k", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        vp = np.stack([w.pool_pages("v", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        ctable = np.full((1, lps[-1] + 1), -1, dtype=np.int32)
+        ctable[0, lps] = np.arange(len(lps), dtype=np.int32)
+        slot = (len(lps) - 1) * 64 + p % 64
+        sample.append((t, p, kp, vp, ctable, slot, (p - lo + 1)))
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(repeats):
+        for (t, p, kp, vp, ctable, slot, nkeys) in sample:
+            q_out, kp2, vp2 = paged.append_rope(q_all[[t]], k_all[[t]], v_all[[t]], tp[[t]], tr[[t]], None,
+                                                kp, vp, inv, slots=np.array([slot]), gamma_q=gq,
+                                                gamma_k=gk, eps=w.norm_eps)
+            paged.attention_at(q_out[0], 0, p, ctable, kp2, vp2, w.window)
+            nbytes += 2 * w.hkv * nkeys * w.head_dim * 2 + 2 * w.hq * w.head_dim * 2
+    return time.perf_counter() - t0, nbytes
+
+
+def threads_used():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores, each step a bounded sample of rows."""
+    import synth
+    if rank != 0:
+        return None
+    w = synth.build(args.config)
+    rng = np.random.default_rng(0)
+    rows = sorted(rng.choice(w.B, size=min(w.B, args.ref_rows), replace=False).tolist())
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_sample(w, rows[:1])
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        s, nb = cpu_oracle_sample(w, rows)
+        secs += s
+        nbytes += nb
+    value = nbytes / secs / 1e9
+    cores = threads_used()
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * secs / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.config, "description": CONFIGS[args.config],
+                   "sample_rows_per_step": len(rows)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(rows)} decode rows of the {args.config} workload per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+
+    import paged_kv_gqa_row_gb300 as lnk
+    import synth
+    from synth import device as sdev
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    seed = None if rank == 0 else 1000 + 97 * rank + {"phi3_tiny": 1, "mistral": 2, "phi3_window": 3,
+                                                       "qwen3": 4, "llama_step": 5}[args.config]
+    w = synth.build(args.config, seed=seed)
+    parts = algorithmic_bytes(w)
+    pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * 2
+    copies = 2 if pool_bytes < (8 << 30) else 1
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    def d32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    shape = (w.hkv, w.pool_positions, w.head_dim)
+    pools = []
+    for _ in range(copies):
+        kp = torch.empty(shape, dtype=torch.int16, device=dev)
+        vp = torch.empty(shape, dtype=torch.int16, device=dev)
+        sdev.fill_normal_bf16(kp, w.pool_key("k"))
+        sdev.fill_normal_bf16(vp, w.pool_key("v"))
+        pools.append((kp, vp))
+    q, k, v = d16(w.step_q()), d16(w.step_k()), d16(w.step_v())
+    pos, rows, table = d32(w.token_positions()), d32(w.token_rows()), d32(w.table)
+    dec_pos = d32(w.dec_positions)
+    ch = (d32(w.ch_rows), d32(w.ch_positions), d32(w.ch_segments)) if w.P else (None, None, None)
+    gq = None if w.gamma_q() is None else d16(w.gamma_q())
+    gk = None if w.gamma_k() is None else d16(w.gamma_k())
+    q_out = torch.zeros_like(q)
+    out = torch.zeros_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row, window=w.window)
+    rd = lnk.rope_desc(w.theta, w.llama3)
+    ws_bytes = lnk.lnk_paged_workspace_size(desc, max(1, w.B))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    s_handle = stream.cuda_stream
+    row_elems = w.hq * w.head_dim
+
+    def attend(kp, vp, q_src, out_dst):
+        if w.P == 0:
+            lnk.lnk_paged_decode_attn(desc, q_src, dec_pos, table, kp, vp, out_dst, w.B, ws, ws_bytes,
+                                      status, s_handle)
+        else:
+            lnk.lnk_paged_step_attn(desc, q_src, ch[0], ch[1], ch[2], dec_pos, table, kp, vp, out_dst,
+                                    None, None, w.P, w.B, 0, ws, ws_bytes, status, s_handle)
+
+    def step(i, ev=None):
+        kp, vp = pools[i % copies]
+        lnk.lnk_paged_append_rope(desc, rd, q, k, v, pos, rows, None, table, gq, gk, w.norm_eps, kp, vp,
+                                  q_out, w.T, status, s_handle)
+        if ev is not None:
+            ev[0].record(stream)
+        attend(kp, vp, q_out, out)
+        if ev is not None:
+            ev[1].record(stream)
+
+    launches_per_step = 1 + (1 if w.P else 0) + (2 if w.B else 0)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_on()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, dec_events[i])
+        t_end.record(stream)
+    stream.synchronize()
+    if sampler:
+        sampler.mark_off()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_events]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    clocks = sampler.stop() if sampler else None
+
+    # ---- end to end: host buffers in, result out, through the same C ABI ----
+    h_q = torch.from_numpy(w.step_q().view(np.int16)).pin_memory()
+    h_k = torch.from_numpy(w.step_k().view(np.int16)).pin_memory()
+    h_v = torch.from_numpy(w.step_v().view(np.int16)).pin_memory()
+    h_pos = torch.from_numpy(w.token_positions().astype(np.int32)).pin_memory()
+    h_table = torch.from_numpy(np.ascontiguousarray(w.table, dtype=np.int32)).pin_memory()
+    h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pos, h_table))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step(i):
+        q.copy_(h_q, non_blocking=True)
+        k.copy_(h_k, non_blocking=True)
+        v.copy_(h_v, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        table.copy_(h_table, non_blocking=True)
+        step(i)
+        h_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+
+    vals = torch.tensor([elapsed_ms, e2e_ms, dec_avg_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms, dec_avg_ms = [float(x) for x in vals.tolist()]
+
+    if rank != 0:
+        return None
+    peak, peak_kind = read_peaks()
+    step_bytes = parts["step"]
+    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    e2e_value = world * step_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9
+    dec_bytes = parts["decode_call"]
+    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic = recorded_traffic("decode.cu", args.config)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "description": CONFIGS[args.config],
+                   "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
+                   "head_dim": w.head_dim, "page_size": 64, "num_pages": w.num_pages,
+                   "parallelism": f"rows x{world} (independent batches per GPU)",
+                   "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e9:.2f} GB, "
+                         "alternated step to step",
+                   "algorithmic_bytes_per_step": step_bytes},
+        "row_steps_per_s": round(world * w.B * args.steps / (elapsed_ms / 1e3), 1),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "lnk_paged_decode_attn (decode + combine kernels)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes": dec_bytes,
+                     "avg_launch_ms": round(dec_avg_ms, 5)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        rng = np.random.default_rng(0)
+        rows_s = sorted(rng.choice(w.B, size=min(w.B, args.ref_rows), replace=False).tolist())
+        secs, nb, reps = 0.0, 0, 0
+        while secs < args.cpu_seconds and reps < 50:
+            s, b = cpu_oracle_sample(w, rows_s)
+            secs += s
+            nb += b
+            reps += 1
+        line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": threads_used(),
+                                "kind": "oracle",
+                                "sample": f"{len(rows_s)} decode rows x {reps} repeats of the {args.config} "
+                                          f"workload ({secs:.1f} s)"}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="mistral", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="lnk", choices=["lnk", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend)
+        dist = tdist
+    if args.impl == "reference":
+        args.steps = min(args.steps, 10)
+        line = run_reference(args, rank, world)
+    else:
+        line = run_gpu(args, rank, world, dist)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

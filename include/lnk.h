@@ -1,0 +1,214 @@
+/*
+ * lnk.h -- C ABI of liblnk: paged decode / step attention for GB300 (sm_103a).
+ *
+ * One layer's attention step of a paged decoder-serving engine:
+ *
+ *   lnk_paged_append_rope   rotate the step's q/k with RoPE (after an optional
+ *                           per-head QK-norm) and write each token's k/v into
+ *                           its slot of the shared page pool;
+ *   lnk_paged_decode_attn   one query token per decode row over that row's pages
+ *                           (the serving step "decode_paged");
+ *   lnk_paged_step_attn     packed prompt chunks plus decode rows in one call
+ *                           ("step_paged"; with no decode rows it is
+ *                           "prefill_paged").
+ *
+ * Sources: the model pages "Mistral 7B Instruct v0.3", "Qwen3-4B" and
+ * "Llama 3.1 8B Instruct", Entries table (prefill_paged, decode_paged,
+ * step_paged); "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
+ * (decode_rows, prefill_packed, step_packed, window_mask) and src/rope.linnet
+ * (tables); "Llama 3.1 8B Instruct", rope-scaling paragraph; "Qwen3-4B",
+ * QK-norm paragraph.
+ *
+ * Conventions (all entry points)
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (lnk_bf16), row-major and
+ *     contiguous in the stated shape.  int32 arrays are contiguous.
+ *   - Every pointer argument named "device" is device memory owned by the
+ *     caller; the library allocates nothing, frees nothing and never
+ *     synchronises.  Work is enqueued on `stream` (NULL = legacy default).
+ *   - Pool layout: k_pool and v_pool are [num_kv_heads][num_pages * 64][head_dim]
+ *     bf16 (the caches' [Batch = 1, KvHeads, MaxSeq, D] with MaxSeq =
+ *     num_pages * 64).  Logical position j of table row r lives in pool slot
+ *     table[r * pages_per_row + j / 64] * 64 + j % 64.  Pool pointers must be
+ *     16-byte aligned.
+ *   - Host-detectable argument errors return a status synchronously and
+ *     enqueue nothing.  Data-dependent errors found on the device (a table
+ *     entry outside [0, num_pages), a position past the table row, a bad row
+ *     or slot) make the affected token or page skip its work and OR a
+ *     LNK_DEV_* bit into *dev_status (an int32 in device memory; NULL = do
+ *     not report).  No kernel traps or faults on bad data.
+ *   - A negative position marks an inactive token or row: nothing is written
+ *     for it and its outputs are zero.  This is not an error.
+ *   - Ordering: attention reads the slots append_rope writes, so call
+ *     append_rope first on the same stream.
+ */
+#ifndef LNK_H
+#define LNK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lnk_bf16;          /* bfloat16 bit pattern */
+typedef struct CUstream_st* lnk_stream; /* same type as cudaStream_t */
+
+typedef enum lnk_status {
+  LNK_OK = 0,
+  LNK_EINVAL = 1,          /* null pointer, misaligned pointer, inconsistent shape */
+  LNK_ERANGE = 2,          /* a size outside the supported range */
+  LNK_ECUDA = 3,           /* a CUDA runtime call failed (launch, attribute, ...) */
+  LNK_EUNSUPPORTED = 4,    /* head_dim, group size or page size not supported */
+  LNK_EWORKSPACE = 5       /* workspace NULL or smaller than lnk_paged_workspace_size */
+} lnk_status;
+
+/* Bits ORed into *dev_status by the kernels. */
+#define LNK_DEV_BAD_ROW      0x01  /* a token's row outside [0, num_rows) */
+#define LNK_DEV_BAD_POSITION 0x02  /* position >= pages_per_row * 64 */
+#define LNK_DEV_BAD_PAGE     0x04  /* a table entry outside [0, num_pages) on a read or write path */
+#define LNK_DEV_BAD_SLOT     0x08  /* slots[t] outside [0, num_pages * 64) */
+#define LNK_DEV_SEGMENT      0x10  /* adjacent chunk tokens share a segment but not a row */
+#define LNK_DEV_BAD_LAST     0x20  /* last[m] outside [0, P) */
+#define LNK_DEV_TIMEOUT      0x40  /* a pipeline wait gave up (never expected) */
+
+/* Shape of one attention layer and its page pool. */
+typedef struct lnk_attn_desc {
+  int32_t num_q_heads;    /* Hq */
+  int32_t num_kv_heads;   /* Hkv; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8} */
+  int32_t head_dim;       /* D in {64, 96, 128} */
+  int32_t page_size;      /* positions per page; must be 64 */
+  int32_t num_pages;      /* pages in each of k_pool / v_pool */
+  int32_t num_rows;       /* rows of table */
+  int32_t pages_per_row;  /* columns of table (its row stride, in entries) */
+  int32_t window;         /* 0: none; else key j is visible to a query at p
+                             iff p - window < j <= p (itself and window - 1 before) */
+  float scale;            /* softmax scale; 0 selects 1 / sqrt(head_dim) */
+} lnk_attn_desc;
+
+/* Rotary frequencies: inv_freq[i] = exp(-(f32(i) * 2 / f32(D)) * log(theta))
+ * in float32 ("Phi-3 Mini 4K Instruct -- files", src/rope.linnet, tables),
+ * optionally rescaled by wavelength in three bands ("Llama 3.1 8B Instruct",
+ * rope-scaling paragraph): wavelen > orig / low_freq_factor -> inv / factor;
+ * wavelen < orig / high_freq_factor -> inv; else linear blend with
+ * smooth = (orig / wavelen - low) / (high - low). */
+typedef struct lnk_rope_desc {
+  double theta;                   /* rotary base (as float32, like the pages) */
+  int32_t llama3;                 /* 0: plain; 1: llama3 three-band rescale */
+  double factor;                  /* llama3: 8 for Llama 3.1 */
+  double low_freq_factor;         /* llama3: 1 */
+  double high_freq_factor;        /* llama3: 4 */
+  double original_max_position;   /* llama3: 8192 */
+} lnk_rope_desc;
+
+/* Human-readable name of a status. */
+const char* lnk_status_string(lnk_status status);
+
+/* Host-only: the float32 frequency table the append kernel uses, written to
+ * out[0 .. head_dim/2).  Same definition as lnk_rope_desc's comment; log and
+ * exp are taken correctly rounded, the llama3 rescale in double rounded once. */
+lnk_status lnk_rope_inv_freq(const lnk_rope_desc* rope, int32_t head_dim, float* out);
+
+/* Bytes of device workspace that decode_attn / step_attn need for up to
+ * max_rows decode rows on the current device.  Returns 0 on bad arguments. */
+size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows);
+
+/*
+ * lnk_paged_append_rope -- per token: optional QK-norm, RoPE, K/V append.
+ *
+ * Defines: "Qwen3-4B" QK-norm paragraph (RMS over each head's head_dim slice,
+ * eps, weight gamma, after the head split, before rope); "Phi-3 Mini 4K
+ * Instruct -- files" src/rope.linnet tables (angle f32(position) * inv_freq[i],
+ * each frequency used for both halves: element i turns with element i + D/2)
+ * and src/attention.linnet write_tokens; "Mistral 7B Instruct v0.3" Entries
+ * table, prefill_paged ("each token written at its place in the pool").
+ *
+ *   q        device [T][Hq][D]   projected queries
+ *   k, v     device [T][Hkv][D]  projected keys / values
+ *   positions device int32 [T]   position of each token in its row (< 0: inactive)
+ *   rows     device int32 [T]    table row of each token; NULL: token t uses row t
+ *   slots    device int32 [T]    pool slot to write; NULL: derived from the table
+ *   table    device int32 [num_rows][pages_per_row] (unused when slots != NULL)
+ *   q_norm_w, k_norm_w  device [D] QK-norm weights, or NULL for no QK-norm
+ *   norm_eps QK-norm epsilon (1e-6 for Qwen3)
+ *   k_pool, v_pool  device pools (written at the tokens' slots only)
+ *   q_out    device [T][Hq][D]   rotated queries (zero for inactive tokens)
+ *   T        tokens (0 is allowed and enqueues nothing)
+ *
+ * Numerics: QK-norm, cos/sin of the float32 angle and the rotation are
+ * evaluated in double precision and rounded once to bf16 (nearest even);
+ * v is copied bit for bit.  Two tokens writing one slot race (the engine's
+ * padding tokens write a shared dump slot nobody reads).
+ */
+lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope,
+                                 const lnk_bf16* q, const lnk_bf16* k, const lnk_bf16* v,
+                                 const int32_t* positions, const int32_t* rows,
+                                 const int32_t* slots, const int32_t* table,
+                                 const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w,
+                                 float norm_eps, lnk_bf16* k_pool, lnk_bf16* v_pool,
+                                 lnk_bf16* q_out, int32_t T, int32_t* dev_status,
+                                 lnk_stream stream);
+
+/*
+ * lnk_paged_decode_attn -- one query token per decode row over its pages.
+ *
+ * Defines: "Mistral 7B Instruct v0.3" Entries table, decode_paged ("decode_rows
+ * for serving from pages"); "Phi-3 Mini 4K Instruct -- files",
+ * src/attention.linnet decode_rows (row b attends over itself up to
+ * positions[b], with the window mask) and the scale rsqrt(head_dim).
+ * Query head h reads kv head h / (Hq / Hkv).
+ *
+ *   q_roped  device [B][Hq][D]  rotated queries (q_out of append_rope)
+ *   positions device int32 [B]  position of row b's token (< 0: inactive row)
+ *   table    device int32 [num_rows][pages_per_row]; decode row b uses table row b
+ *   k_pool, v_pool device pools
+ *   out      device [B][Hq][D]  attention output (bf16, nearest even)
+ *   B        decode rows, 0 <= B <= min(num_rows, 4096)
+ *   workspace device scratch of ws_bytes >= lnk_paged_workspace_size(desc, B)
+ *             (256-byte aligned; contents need no initialisation)
+ */
+lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
+                                 const int32_t* positions, const int32_t* table,
+                                 const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                                 lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes,
+                                 int32_t* dev_status, lnk_stream stream);
+
+/*
+ * lnk_paged_step_attn -- packed prompt chunks and decode rows in one call.
+ *
+ * Defines: "Mistral 7B Instruct v0.3" Entries table, step_paged ("prefill_paged
+ * and decode_paged in one pass") and prefill_paged (prompts packed end to end,
+ * each token attending over its row's pages up to its position: chunks,
+ * shared prefixes); "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
+ * step_packed / prefill_packed (prompt tokens first, then one token per row)
+ * and src/lib.linnet prefill_packed (last[m] names prompt m's last token).
+ *
+ *   q_roped   device [P + B][Hq][D]: P chunk tokens, then B decode rows
+ *   rows      device int32 [P]  table row of each chunk token
+ *   positions device int32 [P]  position of each chunk token (< 0: inactive)
+ *   segments  device int32 [P]  prompt of each chunk token, or NULL.  Prompts
+ *             live in their own rows, so a token sees only its own prompt (and
+ *             that row's earlier context); adjacent tokens with equal segments
+ *             must share a row (LNK_DEV_SEGMENT otherwise).
+ *   step_positions device int32 [B]  decode row b's position; row b uses table row b
+ *   table, k_pool, v_pool  as above
+ *   out       device [P + B][Hq][D]
+ *   last      device int32 [M] or NULL: chunk token whose output row is copied
+ *             to last_out[m] (device [M][Hq][D]); M may be 0
+ *   P, B      chunk tokens and decode rows (either may be 0)
+ *   workspace as for decode_attn with max_rows >= B
+ */
+lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
+                               const int32_t* rows, const int32_t* positions,
+                               const int32_t* segments, const int32_t* step_positions,
+                               const int32_t* table, const lnk_bf16* k_pool,
+                               const lnk_bf16* v_pool, lnk_bf16* out, const int32_t* last,
+                               lnk_bf16* last_out, int32_t P, int32_t B, int32_t M,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               lnk_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LNK_H */

@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) paged decode / step attention.
+
+The product is the C-ABI library ``liblnk.so`` (declared in ``include/lnk.h``);
+this package holds its CUDA sources (``csrc/``), the build step (``build.py``)
+and a thin ctypes binding with the C names (``binding.py``).
+"""
+from .binding import (  # noqa: F401
+    EXPORTED,
+    LIBRARY_PATH,
+    AttnDesc,
+    LnkError,
+    RopeDesc,
+    attn_desc,
+    lnk_paged_append_rope,
+    lnk_paged_decode_attn,
+    lnk_paged_step_attn,
+    lnk_paged_workspace_size,
+    lnk_rope_inv_freq,
+    lnk_status_string,
+    rope_desc,
+)

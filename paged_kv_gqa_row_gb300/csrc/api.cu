@@ -1,0 +1,311 @@
+// C ABI entry points of liblnk: argument checks, frequency tables, tensor
+// maps and launches.  Nothing here allocates device memory or synchronises.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace lnk {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int g_sm_count[kMaxDevices];
+std::once_flag g_sm_once[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Tensor map over one pool: rows = kv_heads * num_pages * 64 positions, each
+// head_dim bf16 wide; boxes of 64 positions x 64 elements, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, const lnk_attn_desc& d) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                        static_cast<cuuint64_t>(d.num_kv_heads) * d.num_pages * kPage};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+  cuuint32_t box[2] = {kBoxCols, kPage};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by every entry point.
+lnk_status check_desc(const lnk_attn_desc* d) {
+  if (d == nullptr) return LNK_EINVAL;
+  if (d->page_size != kPage) return LNK_EUNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128) return LNK_EUNSUPPORTED;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_q_heads % d->num_kv_heads != 0) return LNK_EINVAL;
+  const int g = d->num_q_heads / d->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return LNK_EUNSUPPORTED;
+  if (d->num_pages <= 0 || d->num_rows <= 0 || d->pages_per_row <= 0) return LNK_EINVAL;
+  if (d->window < 0 || !(d->scale >= 0.f)) return LNK_EINVAL;
+  // TMA row coordinates and 32-bit position arithmetic must not overflow
+  if (static_cast<long long>(d->num_kv_heads) * d->num_pages * kPage >= (1ll << 31)) return LNK_ERANGE;
+  if (static_cast<long long>(d->pages_per_row) * kPage >= (1ll << 31)) return LNK_ERANGE;
+  if (static_cast<long long>(d->num_rows) * d->pages_per_row >= (1ll << 31)) return LNK_ERANGE;
+  return LNK_OK;
+}
+
+float scale_log2(const lnk_attn_desc* d) {
+  const double s = d->scale > 0.f ? static_cast<double>(d->scale) : 1.0 / std::sqrt(static_cast<double>(d->head_dim));
+  return static_cast<float>(s * 1.4426950408889634);  // log2(e)
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::call_once(g_sm_once[dev], [dev] {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n;
+  });
+  return g_sm_count[dev];
+}
+
+// Frequency table of lnk_rope_desc (float32 operations as the pages write them).
+static lnk_status inv_freq_table(const lnk_rope_desc* rope, int head_dim, float* out) {
+  if (rope == nullptr || out == nullptr || head_dim <= 0 || head_dim % 2 || head_dim > 128) return LNK_EINVAL;
+  if (!(rope->theta > 1.0)) return LNK_EINVAL;
+  const float theta32 = static_cast<float>(rope->theta);
+  const float log_theta = static_cast<float>(std::log(static_cast<double>(theta32)));
+  const float d32 = static_cast<float>(head_dim);
+  for (int i = 0; i < head_dim / 2; ++i) {
+    volatile float t = static_cast<float>(i) * 2.0f;  // volatile: keep each float32 rounding
+    volatile float u = t / d32;
+    volatile float e = (-u) * log_theta;
+    out[i] = static_cast<float>(std::exp(static_cast<double>(e)));
+  }
+  if (rope->llama3) {
+    const double factor = rope->factor, low = rope->low_freq_factor, high = rope->high_freq_factor;
+    const double orig = rope->original_max_position;
+    if (!(factor > 0.0) || !(high > low) || !(orig > 0.0)) return LNK_EINVAL;
+    const double two_pi = 2.0 * 3.14159265358979323846;
+    for (int i = 0; i < head_dim / 2; ++i) {
+      const double inv = static_cast<double>(out[i]);
+      const double wavelen = two_pi / inv;
+      double v;
+      if (wavelen > orig / low) {
+        v = inv / factor;
+      } else if (wavelen < orig / high) {
+        v = inv;
+      } else {
+        const double smooth = (orig / wavelen - low) / (high - low);
+        volatile double a = (1.0 - smooth) * (inv / factor);
+        volatile double b = smooth * inv;
+        v = a + b;
+      }
+      out[i] = static_cast<float>(v);
+    }
+  }
+  return LNK_OK;
+}
+
+}  // namespace lnk
+
+using namespace lnk;
+
+extern "C" {
+
+const char* lnk_status_string(lnk_status s) {
+  switch (s) {
+    case LNK_OK: return "LNK_OK";
+    case LNK_EINVAL: return "LNK_EINVAL: invalid argument";
+    case LNK_ERANGE: return "LNK_ERANGE: size out of range";
+    case LNK_ECUDA: return "LNK_ECUDA: CUDA runtime error";
+    case LNK_EUNSUPPORTED: return "LNK_EUNSUPPORTED: unsupported shape";
+    case LNK_EWORKSPACE: return "LNK_EWORKSPACE: workspace missing or too small";
+  }
+  return "unknown lnk_status";
+}
+
+lnk_status lnk_rope_inv_freq(const lnk_rope_desc* rope, int32_t head_dim, float* out) {
+  return inv_freq_table(rope, head_dim, out);
+}
+
+size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows) {
+  if (check_desc(desc) != LNK_OK || max_rows < 0 || max_rows > kMaxDecodeRows) return 0;
+  const int grid = device_sm_count();
+  if (grid <= 0) return 0;
+  return decode_workspace_layout(max_rows, desc->num_kv_heads, desc->num_q_heads / desc->num_kv_heads,
+                                 desc->head_dim, grid)
+      .total;
+}
+
+lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope, const lnk_bf16* q,
+                                 const lnk_bf16* k, const lnk_bf16* v, const int32_t* positions,
+                                 const int32_t* rows, const int32_t* slots, const int32_t* table,
+                                 const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w, float norm_eps,
+                                 lnk_bf16* k_pool, lnk_bf16* v_pool, lnk_bf16* q_out, int32_t T,
+                                 int32_t* dev_status, lnk_stream stream) {
+  lnk_status st = check_desc(desc);
+  if (st != LNK_OK) return st;
+  if (T < 0) return LNK_EINVAL;
+  if (T == 0) return LNK_OK;
+  if (!q || !k || !v || !positions || !k_pool || !v_pool || !q_out) return LNK_EINVAL;
+  if (slots == nullptr && table == nullptr) return LNK_EINVAL;
+  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 16) || !aligned(q_out, 4) || !aligned(k_pool, 16) ||
+      !aligned(v_pool, 16) || (q_norm_w && !aligned(q_norm_w, 4)) || (k_norm_w && !aligned(k_norm_w, 4)))
+    return LNK_EINVAL;
+  if ((q_norm_w || k_norm_w) && !(norm_eps >= 0.f)) return LNK_EINVAL;
+  if (rows == nullptr && slots == nullptr && T > desc->num_rows) return LNK_EINVAL;
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  st = inv_freq_table(rope, desc->head_dim, p.inv_freq);
+  if (st != LNK_OK) return st;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.positions = positions;
+  p.rows = rows;
+  p.slots = slots;
+  p.table = table;
+  p.q_norm_w = q_norm_w;
+  p.k_norm_w = k_norm_w;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.q_out = q_out;
+  p.status = dev_status;
+  p.norm_eps = static_cast<double>(norm_eps);
+  p.T = T;
+  p.hq = desc->num_q_heads;
+  p.hkv = desc->num_kv_heads;
+  p.num_pages = desc->num_pages;
+  p.num_rows = desc->num_rows;
+  p.pages_per_row = desc->pages_per_row;
+  return launch_append(p, desc->head_dim, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? LNK_OK
+                                                                                                : LNK_ECUDA;
+}
+
+static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, const int32_t* positions,
+                                const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                                lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+  if (B == 0) return LNK_OK;
+  DecodeLaunch launch;
+  if (decode_prepare(desc->head_dim, B, &launch) != cudaSuccess || launch.grid <= 0) return LNK_ECUDA;
+  const int group = desc->num_q_heads / desc->num_kv_heads;
+  const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
+  if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 256)) return LNK_EWORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p;
+  p.q = q;
+  p.positions = positions;
+  p.table = table;
+  p.out = out;
+  p.status = dev_status;
+  p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
+  p.ws_pref = reinterpret_cast<int32_t*>(ws + w.pref);
+  p.ws_ml = reinterpret_cast<float*>(ws + w.ml);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o);
+  p.B = B;
+  p.hq = desc->num_q_heads;
+  p.hkv = desc->num_kv_heads;
+  p.group = group;
+  p.num_pages = desc->num_pages;
+  p.pages_per_row = desc->pages_per_row;
+  p.window = desc->window;
+  p.scale_log2 = scale_log2(desc);
+  return launch_decode(kmap, vmap, p, desc->head_dim, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
+}
+
+lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
+                                 const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                                 lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 lnk_stream stream) {
+  lnk_status st = check_desc(desc);
+  if (st != LNK_OK) return st;
+  if (B < 0 || B > desc->num_rows) return LNK_EINVAL;
+  if (B > kMaxDecodeRows) return LNK_ERANGE;
+  if (B == 0) return LNK_OK;
+  if (!q_roped || !positions || !table || !k_pool || !v_pool || !out) return LNK_EINVAL;
+  if (!aligned(q_roped, 4) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
+  CUtensorMap kmap, vmap;
+  if (!make_pool_map(&kmap, k_pool, *desc) || !make_pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
+  return decode_common(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
+                       kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* rows,
+                               const int32_t* positions, const int32_t* segments, const int32_t* step_positions,
+                               const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                               lnk_bf16* out, const int32_t* last, lnk_bf16* last_out, int32_t P, int32_t B,
+                               int32_t M, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               lnk_stream stream) {
+  lnk_status st = check_desc(desc);
+  if (st != LNK_OK) return st;
+  if (P < 0 || B < 0 || M < 0 || B > desc->num_rows) return LNK_EINVAL;
+  if (B > kMaxDecodeRows) return LNK_ERANGE;
+  if (P == 0 && B == 0) return LNK_OK;
+  if (!q_roped || !table || !k_pool || !v_pool || !out) return LNK_EINVAL;
+  if (P > 0 && (!rows || !positions)) return LNK_EINVAL;
+  if (B > 0 && !step_positions) return LNK_EINVAL;
+  if (M > 0 && (!last || !last_out)) return LNK_EINVAL;
+  if (!aligned(q_roped, 4) || !aligned(out, 4) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
+  if (B > 0) {
+    const size_t need = lnk_paged_workspace_size(desc, B);
+    if (workspace == nullptr || need == 0 || ws_bytes < need) return LNK_EWORKSPACE;
+  }
+  CUtensorMap kmap, vmap;
+  if (!make_pool_map(&kmap, k_pool, *desc) || !make_pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int group = desc->num_q_heads / desc->num_kv_heads;
+  const size_t row_elems = static_cast<size_t>(desc->num_q_heads) * desc->head_dim;
+  if (P > 0) {
+    ChunkParams c;
+    c.q = q_roped;
+    c.rows = rows;
+    c.positions = positions;
+    c.segments = segments;
+    c.table = table;
+    c.out = out;
+    c.status = dev_status;
+    c.P = P;
+    c.hq = desc->num_q_heads;
+    c.hkv = desc->num_kv_heads;
+    c.group = group;
+    c.num_pages = desc->num_pages;
+    c.num_rows = desc->num_rows;
+    c.pages_per_row = desc->pages_per_row;
+    c.window = desc->window;
+    c.tile_tokens = 128 / group;
+    c.num_tiles = (P + c.tile_tokens - 1) / c.tile_tokens;
+    c.scale_log2 = scale_log2(desc);
+    if (launch_chunk(kmap, vmap, c, desc->head_dim, s) != cudaSuccess) return LNK_ECUDA;
+  }
+  if (B > 0) {
+    st = decode_common(desc, q_roped + static_cast<size_t>(P) * row_elems, step_positions, table, k_pool, v_pool,
+                       out + static_cast<size_t>(P) * row_elems, B, workspace, ws_bytes, dev_status, kmap, vmap, s);
+    if (st != LNK_OK) return st;
+  }
+  if (M > 0) {
+    if (launch_gather_last(out, last, last_out, M, P, static_cast<int>(row_elems), dev_status, s) != cudaSuccess)
+      return LNK_ECUDA;
+  }
+  return LNK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// Kernel parameter blocks and launchers shared by the translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/lnk.h"
+
+namespace lnk {
+
+constexpr int kPage = 64;          // positions per page
+constexpr int kBoxCols = 64;       // bf16 elements per TMA box row (128 bytes)
+constexpr int kBoxBytes = kPage * kBoxCols * 2;  // one 64 x 64 bf16 box: 8 KiB
+constexpr int kMaxDecodeRows = 4096;
+constexpr int kMaxGroup = 8;
+
+__host__ __device__ constexpr int boxes_for(int d) { return (d + kBoxCols - 1) / kBoxCols; }
+
+// ---------------------------------------------------------------- append --
+struct AppendParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* positions;
+  const int32_t* rows;
+  const int32_t* slots;
+  const int32_t* table;
+  const uint16_t* q_norm_w;
+  const uint16_t* k_norm_w;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  uint16_t* q_out;
+  int32_t* status;
+  double norm_eps;
+  int T, hq, hkv, num_pages, num_rows, pages_per_row;
+  float inv_freq[64];
+};
+
+cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode --
+struct DecodeParams {
+  const uint16_t* q;          // [B][Hq][D]
+  const int32_t* positions;   // [B]
+  const int32_t* table;       // [num_rows][pages_per_row]
+  uint16_t* out;              // [B][Hq][D]
+  int32_t* status;
+  int32_t* ws_meta;           // [0] = page-heads per CTA
+  int32_t* ws_pref;           // [B + 1] prefix sums of visible pages per row
+  float* ws_ml;               // [segments][G][2]: running max (log2 units), sum
+  float* ws_o;                // [segments][G][D]: unnormalised partial outputs
+  int B, hq, hkv, group, num_pages, pages_per_row, window;
+  float scale_log2;           // softmax scale * log2(e)
+};
+
+struct DecodeLaunch {
+  int grid;        // persistent CTAs
+  int smem_bytes;  // dynamic shared memory per CTA
+};
+
+// Workspace layout for `rows` decode rows and `grid` CTAs (byte offsets).
+struct DecodeWorkspace {
+  size_t meta, pref, ml, o, total;
+};
+DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
+
+cudaError_t decode_prepare(int head_dim, int B, DecodeLaunch* launch);
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                          int head_dim, const DecodeLaunch& launch, cudaStream_t stream);
+
+// ----------------------------------------------------------------- chunk --
+struct ChunkParams {
+  const uint16_t* q;          // [P][Hq][D]
+  const int32_t* rows;        // [P]
+  const int32_t* positions;   // [P]
+  const int32_t* segments;    // [P] or null
+  const int32_t* table;
+  uint16_t* out;              // [P][Hq][D]
+  int32_t* status;
+  int P, hq, hkv, group, num_pages, num_rows, pages_per_row, window;
+  int tile_tokens, num_tiles;
+  float scale_log2;
+};
+
+cudaError_t launch_chunk(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
+                         int head_dim, cudaStream_t stream);
+
+// ------------------------------------------------------------ gather last --
+cudaError_t launch_gather_last(const uint16_t* out, const int32_t* last, uint16_t* last_out, int M,
+                               int P, int row_elems, int32_t* status, cudaStream_t stream);
+
+// ------------------------------------------------------------- device info --
+int device_sm_count();
+
+}  // namespace lnk
