@@ -263,7 +263,7 @@ def run_gpu(args, rank, world, dist):
     w = synth.build(args.config, seed=seed)
     parts = algorithmic_bytes(w)
     pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * 2
-    copies = 2 if pool_bytes < (8 << 30) else 1
+    copies = args.pool_copies or (2 if pool_bytes < (8 << 30) else 1)
 
     def d16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
@@ -451,6 +451,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-copies", type=int, default=0, help="pool copies alternated step to step (0: auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
