@@ -291,35 +291,37 @@ def run_gpu(args, rank, world, dist):
     desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row, window=w.window)
     rd = lnk.rope_desc(w.theta, w.llama3)
     ws_bytes = lnk.lnk_paged_workspace_size(desc, max(1, w.B))
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     s_handle = stream.cuda_stream
     row_elems = w.hq * w.head_dim
 
-    def attend(kp, vp, q_src, out_dst):
+    def attend(kp, vp, q_src, out_dst, tab):
         if w.P == 0:
-            lnk.lnk_paged_decode_attn(desc, q_src, dec_pos, table, kp, vp, out_dst, w.B, ws, ws_bytes,
+            lnk.lnk_paged_decode_attn(desc, q_src, dec_pos, tab, kp, vp, out_dst, w.B, ws, ws_bytes,
                                       status, s_handle)
         else:
-            lnk.lnk_paged_step_attn(desc, q_src, ch[0], ch[1], ch[2], dec_pos, table, kp, vp, out_dst,
+            lnk.lnk_paged_step_attn(desc, q_src, ch[0], ch[1], ch[2], dec_pos, tab, kp, vp, out_dst,
                                     None, None, w.P, w.B, 0, ws, ws_bytes, status, s_handle)
 
-    def step(i, ev=None):
+    def step(i, inp, ev=None):
+        qq, kk, vv, pp, tab = inp
         kp, vp = pools[i % copies]
-        lnk.lnk_paged_append_rope(desc, rd, q, k, v, pos, rows, None, table, gq, gk, w.norm_eps, kp, vp,
+        lnk.lnk_paged_append_rope(desc, rd, qq, kk, vv, pp, rows, None, tab, gq, gk, w.norm_eps, kp, vp,
                                   q_out, w.T, status, s_handle)
         if ev is not None:
             ev[0].record(stream)
-        attend(kp, vp, q_out, out)
+        attend(kp, vp, q_out, out, tab)
         if ev is not None:
             ev[1].record(stream)
 
-    launches_per_step = 1 + (1 if w.P else 0) + (2 if w.B else 0)
+    inputs = (q, k, v, pos, table)
+    launches_per_step = 1 + (1 if w.P else 0) + (1 if w.B else 0)
 
     # warm-up
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            step(i, inputs)
     stream.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
 
@@ -338,7 +340,7 @@ def run_gpu(args, rank, world, dist):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(args.steps):
-            step(i, dec_events[i])
+            step(i, inputs, dec_events[i])
         t_end.record(stream)
     stream.synchronize()
     if sampler:
@@ -351,24 +353,31 @@ def run_gpu(args, rank, world, dist):
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     clocks = sampler.stop() if sampler else None
 
-    # ---- end to end: host buffers in, result out, through the same C ABI ----
-    h_q = torch.from_numpy(w.step_q().view(np.int16)).pin_memory()
-    h_k = torch.from_numpy(w.step_k().view(np.int16)).pin_memory()
-    h_v = torch.from_numpy(w.step_v().view(np.int16)).pin_memory()
-    h_pos = torch.from_numpy(w.token_positions().astype(np.int32)).pin_memory()
-    h_table = torch.from_numpy(np.ascontiguousarray(w.table, dtype=np.int32)).pin_memory()
+    # ---- end to end: the step's inputs from pinned host memory (one packed
+    # buffer, one copy), the C ABI calls, and the result copied back ----
+    host_parts = [w.step_q().view(np.uint8).ravel(), w.step_k().view(np.uint8).ravel(),
+                  w.step_v().view(np.uint8).ravel(), w.token_positions().astype(np.int32).view(np.uint8),
+                  np.ascontiguousarray(w.table, dtype=np.int32).view(np.uint8).ravel()]
+    offs = np.cumsum([0] + [((a.size + 255) // 256) * 256 for a in host_parts])
+    h_in = torch.zeros(int(offs[-1]), dtype=torch.uint8).pin_memory()
+    for a, o0 in zip(host_parts, offs[:-1]):
+        h_in[int(o0):int(o0) + a.size] = torch.from_numpy(a.copy())
+    d_in = torch.empty_like(h_in, device=dev)
+
+    def view(i, dtype, shape):
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        return d_in[int(offs[i]):int(offs[i]) + n].view(dtype).view(shape)
+
+    e_inputs = (view(0, torch.int16, q.shape), view(1, torch.int16, k.shape), view(2, torch.int16, v.shape),
+                view(3, torch.int32, pos.shape), view(4, torch.int32, table.shape))
     h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pos, h_table))
+    h2d = int(sum(a.size for a in host_parts))
     d2h = h_out.numel() * h_out.element_size()
     e2e_steps = max(1, min(args.steps, 200))
 
     def e2e_step(i):
-        q.copy_(h_q, non_blocking=True)
-        k.copy_(h_k, non_blocking=True)
-        v.copy_(h_v, non_blocking=True)
-        pos.copy_(h_pos, non_blocking=True)
-        table.copy_(h_table, non_blocking=True)
-        step(i)
+        d_in.copy_(h_in, non_blocking=True)
+        step(i, e_inputs)
         h_out.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -386,6 +395,7 @@ def run_gpu(args, rank, world, dist):
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+    assert np.array_equal(h_out.numpy(), out.cpu().numpy()), "end-to-end result differs from the device result"
 
     vals = torch.tensor([elapsed_ms, e2e_ms, dec_avg_ms], dtype=torch.float64, device=dev)
     if dist:
@@ -398,7 +408,7 @@ def run_gpu(args, rank, world, dist):
     step_bytes = parts["step"]
     value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
     e2e_value = world * step_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9
-    dec_bytes = parts["decode_call"]
+    dec_bytes = parts["decode_call"] + (parts["chunk_kv"] + parts["chunk_q_out"] if w.P else 0)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = recorded_traffic("decode.cu", args.config)
     line = {
@@ -415,7 +425,7 @@ def run_gpu(args, rank, world, dist):
                    "algorithmic_bytes_per_step": step_bytes},
         "row_steps_per_s": round(world * w.B * args.steps / (elapsed_ms / 1e3), 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "lnk_paged_decode_attn (decode + combine kernels)",
+        "roofline": {"bound": "hbm", "kernel": ("lnk_paged_step_attn (chunk_kernel + decode_kernel)" if w.P else "lnk_paged_decode_attn (decode_kernel)"),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": dec_bytes,

@@ -110,7 +110,11 @@ const char* lnk_status_string(lnk_status status);
 lnk_status lnk_rope_inv_freq(const lnk_rope_desc* rope, int32_t head_dim, float* out);
 
 /* Bytes of device workspace that decode_attn / step_attn need for up to
- * max_rows decode rows on the current device.  Returns 0 on bad arguments. */
+ * max_rows decode rows on the current device.  Returns 0 on bad arguments.
+ * The workspace must be zero-filled once before its first use (it holds
+ * counters that every completed call leaves at zero); zero it again only after
+ * a call reported LNK_DEV_TIMEOUT.  Calls that share a workspace must not run
+ * concurrently. */
 size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows);
 
 /*
@@ -158,14 +162,14 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  * positions[b], with the window mask) and the scale rsqrt(head_dim).
  * Query head h reads kv head h / (Hq / Hkv).
  *
- *   q_roped  device [B][Hq][D]  rotated queries (q_out of append_rope)
+ *   q_roped  device [B][Hq][D]  rotated queries (q_out of append_rope), 16-byte aligned
  *   positions device int32 [B]  position of row b's token (< 0: inactive row)
  *   table    device int32 [num_rows][pages_per_row]; decode row b uses table row b
  *   k_pool, v_pool device pools
- *   out      device [B][Hq][D]  attention output (bf16, nearest even)
+ *   out      device [B][Hq][D]  attention output (bf16, nearest even), 8-byte aligned
  *   B        decode rows, 0 <= B <= min(num_rows, 4096)
  *   workspace device scratch of ws_bytes >= lnk_paged_workspace_size(desc, B)
- *             (256-byte aligned; contents need no initialisation)
+ *             (256-byte aligned; zero-filled before its first use)
  */
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
                                  const int32_t* positions, const int32_t* table,
@@ -183,7 +187,7 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
  * step_packed / prefill_packed (prompt tokens first, then one token per row)
  * and src/lib.linnet prefill_packed (last[m] names prompt m's last token).
  *
- *   q_roped   device [P + B][Hq][D]: P chunk tokens, then B decode rows
+ *   q_roped   device [P + B][Hq][D]: P chunk tokens, then B decode rows (16-byte aligned)
  *   rows      device int32 [P]  table row of each chunk token
  *   positions device int32 [P]  position of each chunk token (< 0: inactive)
  *   segments  device int32 [P]  prompt of each chunk token, or NULL.  Prompts

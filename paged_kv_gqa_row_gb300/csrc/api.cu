@@ -217,8 +217,7 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.table = table;
   p.out = out;
   p.status = dev_status;
-  p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
-  p.ws_pref = reinterpret_cast<int32_t*>(ws + w.pref);
+  p.ws_count = reinterpret_cast<int32_t*>(ws + w.count);
   p.ws_ml = reinterpret_cast<float*>(ws + w.ml);
   p.ws_o = reinterpret_cast<float*>(ws + w.o);
   p.B = B;
@@ -242,7 +241,7 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
   if (B > kMaxDecodeRows) return LNK_ERANGE;
   if (B == 0) return LNK_OK;
   if (!q_roped || !positions || !table || !k_pool || !v_pool || !out) return LNK_EINVAL;
-  if (!aligned(q_roped, 4) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
+  if (!aligned(q_roped, 16) || !aligned(out, 8) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
   CUtensorMap kmap, vmap;
   if (!make_pool_map(&kmap, k_pool, *desc) || !make_pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
   return decode_common(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
@@ -264,7 +263,7 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
   if (P > 0 && (!rows || !positions)) return LNK_EINVAL;
   if (B > 0 && !step_positions) return LNK_EINVAL;
   if (M > 0 && (!last || !last_out)) return LNK_EINVAL;
-  if (!aligned(q_roped, 4) || !aligned(out, 4) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
+  if (!aligned(q_roped, 16) || !aligned(out, 8) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
   if (B > 0) {
     const size_t need = lnk_paged_workspace_size(desc, B);
     if (workspace == nullptr || need == 0 || ws_bytes < need) return LNK_EWORKSPACE;

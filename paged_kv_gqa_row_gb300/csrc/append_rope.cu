@@ -1,12 +1,20 @@
 // K1: per-token QK-norm (optional), RoPE and K/V append into the page pool.
 //
-// One CTA per token.  The token's cos/sin are computed once (double precision,
-// from the float32 angle f32(position) * inv_freq[i]) into shared memory; then
-// each warp takes whole heads: lane l holds elements (2l, 2l+1) of the first
-// half and (D/2 + 2l, D/2 + 2l + 1) of the second half, so the rotate-half
-// partner of every element sits in the same lane.  QK-norm and the rotation
-// run in double precision and are rounded once to bf16; V is copied bit for
-// bit into the token's pool slot.
+// One CTA per token, 16 warps.  The rotated value of element i (paired with
+// i + D/2) is
+//     o_i       = r (x_i (g_i c_i)       - x_{i+D/2} (g_{i+D/2} s_i))
+//     o_{i+D/2} = r (x_{i+D/2} (g_{i+D/2} c_i) + x_i (g_i s_i))
+// where c_i, s_i are the cosine and sine of the float32 angle
+// f32(position) * inv_freq[i], g the QK-norm weights and r the head's RMS
+// factor 1 / sqrt(mean(x^2) + eps) (g = r = 1 without QK-norm).  The four
+// per-frequency coefficients are evaluated once per token in double precision
+// and kept as pairs of floats (hi + lo); each element is then computed with
+// error-free float products and sums (about 2^-46 relative error) and rounded
+// once to bf16, looking at the low part only to break an exact tie of the high
+// part.  The result is the correctly rounded value of the exact expression
+// except in cases far rarer than one in 10^10, without per-element
+// double-precision arithmetic (which is slow on this GPU).  V is copied bit
+// for bit into the token's pool slot.
 //
 // Sources: "Phi-3 Mini 4K Instruct -- files", src/rope.linnet (tables) and
 // src/attention.linnet (rope + write_tokens in prefill_packed / step_packed);
@@ -17,62 +25,103 @@
 namespace lnk {
 namespace {
 
-__device__ __forceinline__ double bf16_to_double(uint16_t b) {
-  return static_cast<double>(__uint_as_float(static_cast<uint32_t>(b) << 16));
+constexpr int kWarps = 16;
+constexpr int kMaxHeadsPerWarp = 8;  // rotated heads (Hq + Hkv) <= 128
+
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
 }
 
-// double -> bf16 bits, round to nearest even, directly (one rounding).
-__device__ __forceinline__ uint16_t double_to_bf16(double x) {
-  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(x));
-  const uint64_t sign = (u >> 63) << 15;
-  const uint64_t mag = u & 0x7FFFFFFFFFFFFFFFull;
-  if (mag == 0) return static_cast<uint16_t>(sign);
-  const int e = static_cast<int>(mag >> 52) - 1023 + 127;  // bf16 biased exponent
-  if (e <= 0 || e >= 255) {
-    // Outside bf16's normal range (never met at unit-scale data): go through
-    // float32, which handles subnormals and overflow.
-    const uint32_t f = __float_as_uint(__double2float_rn(x));
-    const uint32_t r = f + 0x7FFFu + ((f >> 16) & 1u);
-    return static_cast<uint16_t>(r >> 16);
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ DF split(double v) {
+  const float hi = __double2float_rn(v);
+  return {hi, __double2float_rn(v - static_cast<double>(hi))};
+}
+
+// x * a - y * b for bf16-exact x, y and pair-of-float a, b.
+__device__ __forceinline__ DF dot2(float x, DF a, float y, DF b) {
+  const DF p = two_prod(x, a.hi);
+  const DF q = two_prod(y, b.hi);
+  const DF s = two_sum(p.hi, -q.hi);
+  const float l = __fadd_rn(__fadd_rn(s.lo, __fsub_rn(p.lo, q.lo)),
+                            __fsub_rn(__fmul_rn(x, a.lo), __fmul_rn(y, b.lo)));
+  return two_sum(s.hi, l);
+}
+
+__device__ __forceinline__ DF mul_df(DF a, DF r) {
+  const DF m = two_prod(a.hi, r.hi);
+  const float l = __fadd_rn(m.lo, __fadd_rn(__fmul_rn(a.hi, r.lo), __fmul_rn(a.lo, r.hi)));
+  return two_sum(m.hi, l);
+}
+
+// Round hi + lo (|lo| <= half an ulp of hi, hi = RN(hi + lo)) to bf16, nearest even.
+__device__ __forceinline__ uint32_t df_to_bf16(DF v) {
+  const uint32_t u = __float_as_uint(v.hi);
+  if ((u & 0xFFFFu) == 0x8000u && v.lo != 0.f) {
+    // hi sits exactly between two bf16 values: the low part decides
+    const bool away = (v.lo > 0.f) == (v.hi > 0.f);
+    return (u >> 16) + (away ? 1u : 0u);
   }
-  uint64_t kept = mag >> 45;                      // exponent + 7 fraction bits
-  const uint64_t rem = mag & ((1ull << 45) - 1);
-  const uint64_t half = 1ull << 44;
-  if (rem > half || (rem == half && (kept & 1))) kept += 1;  // carries into the exponent
-  const uint64_t e_d = kept >> 7;
-  const uint64_t frac = kept & 0x7F;
-  const int e_b = static_cast<int>(e_d) - 1023 + 127;
-  if (e_b >= 255) return static_cast<uint16_t>(sign | 0x7F80u);
-  return static_cast<uint16_t>(sign | (static_cast<uint64_t>(e_b) << 7) | frac);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
-__device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
-}
-__device__ __forceinline__ void st_u32(uint16_t* p, uint32_t v) {
-  *reinterpret_cast<uint32_t*>(p) = v;
-}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int D>
-__global__ void __launch_bounds__(256) append_rope_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendParams p) {
   constexpr int H = D / 2;
-  constexpr int kLanes = D / 4;  // lanes that hold data
-  __shared__ double s_cos[H];
-  __shared__ double s_sin[H];
+  constexpr int kLanes = D / 4;  // lanes holding data: two elements of each half
+  // coefficient sets: [0] queries, [1] keys; [.][0] g_i c_i, [1] g_{i+H} s_i,
+  // [2] g_{i+H} c_i, [3] g_i s_i
+  __shared__ DF s_coef[2][4][H];
+  __shared__ DF s_ss[kWarps * kMaxHeadsPerWarp];
+  __shared__ DF s_r[kWarps * kMaxHeadsPerWarp];
   __shared__ long long s_slot;
+
+  // Let the next kernel on the stream start its prologue; it waits for this
+  // grid's writes before reading them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int t = blockIdx.x;
   const int pos = p.positions[t];
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nrot = p.hq + p.hkv;  // rotated heads: queries then keys
+  const bool norm_q = p.q_norm_w != nullptr, norm_k = p.k_norm_w != nullptr;
 
+  // ---- per-token coefficients (double precision, once per frequency) ----
   if (tid < H && pos >= 0) {
     const float a = __fmul_rn(static_cast<float>(pos), p.inv_freq[tid]);
     double s, c;
     sincos(static_cast<double>(a), &s, &c);
-    s_cos[tid] = c;
-    s_sin[tid] = s;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t* w = which == 0 ? p.q_norm_w : p.k_norm_w;
+      double g1 = 1.0, g2 = 1.0;
+      if (w != nullptr) {
+        g1 = static_cast<double>(__uint_as_float(static_cast<uint32_t>(w[tid]) << 16));
+        g2 = static_cast<double>(__uint_as_float(static_cast<uint32_t>(w[tid + H]) << 16));
+      }
+      s_coef[which][0][tid] = split(g1 * c);
+      s_coef[which][1][tid] = split(g2 * s);
+      s_coef[which][2][tid] = split(g2 * c);
+      s_coef[which][3][tid] = split(g1 * s);
+    }
   }
-  if (tid == 0) {
+  if (tid == kWarps * 32 - 1) {
     long long slot = -1;
     int bad = 0;
     if (pos >= 0) {
@@ -100,79 +149,102 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const AppendParams p) 
     if (bad && p.status != nullptr) atomicOr(p.status, bad);
     s_slot = slot;
   }
+
+  // ---- load this warp's rotated heads (all loads in flight together) ----
+  const bool has = lane < kLanes;
+  const int e = 2 * lane;
+  uint32_t xlo[kMaxHeadsPerWarp], xhi[kMaxHeadsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kMaxHeadsPerWarp; ++j) {
+    const int hh = warp + j * kWarps;
+    xlo[j] = xhi[j] = 0u;
+    if (hh < nrot && has && pos >= 0) {
+      const uint16_t* src = hh < p.hq ? p.q + (static_cast<size_t>(t) * p.hq + hh) * D
+                                      : p.k + (static_cast<size_t>(t) * p.hkv + (hh - p.hq)) * D;
+      xlo[j] = *reinterpret_cast<const uint32_t*>(src + e);
+      xhi[j] = *reinterpret_cast<const uint32_t*>(src + H + e);
+    }
+  }
+  // QK-norm: sum of squares per head (squares of bf16 values are exact in float)
+  if (norm_q || norm_k) {
+#pragma unroll
+    for (int j = 0; j < kMaxHeadsPerWarp; ++j) {
+      const int hh = warp + j * kWarps;
+      if (hh >= nrot) break;
+      if (!(hh < p.hq ? norm_q : norm_k)) continue;
+      const float a0 = bf16_lo(xlo[j]), a1 = bf16_hi(xlo[j]), b0 = bf16_lo(xhi[j]), b1 = bf16_hi(xhi[j]);
+      DF acc = two_sum(__fmul_rn(a0, a0), __fmul_rn(a1, a1));
+      DF u = two_sum(__fmul_rn(b0, b0), __fmul_rn(b1, b1));
+      DF v = two_sum(acc.hi, u.hi);
+      acc = two_sum(v.hi, __fadd_rn(v.lo, __fadd_rn(acc.lo, u.lo)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, acc.hi, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, acc.lo, o);
+        const DF w = two_sum(acc.hi, oh);
+        acc = two_sum(w.hi, __fadd_rn(w.lo, __fadd_rn(acc.lo, ol)));
+      }
+      if (lane == 0) s_ss[hh] = acc;
+    }
+  }
+  __syncthreads();
+  // one lane per head computes the RMS factor in double precision
+  if ((norm_q || norm_k) && tid < nrot && pos >= 0 && (tid < p.hq ? norm_q : norm_k)) {
+    const DF ss = s_ss[tid];
+    const double v = (static_cast<double>(ss.hi) + static_cast<double>(ss.lo)) / static_cast<double>(D);
+    s_r[tid] = split(1.0 / sqrt(v + p.norm_eps));
+  }
   __syncthreads();
 
   const long long slot = s_slot;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const bool has = lane < kLanes;
-  const int e = 2 * lane;
-  const int nheads = p.hq + 2 * p.hkv;
   const size_t pool_head_stride = static_cast<size_t>(p.num_pages) * kPage * D;
-
-  for (int hh = warp; hh < nheads; hh += 8) {
-    if (hh >= p.hq + p.hkv) {
-      // value head: bit copy into the slot
+#pragma unroll
+  for (int j = 0; j < kMaxHeadsPerWarp; ++j) {
+    const int hh = warp + j * kWarps;
+    if (hh >= nrot) break;
+    const bool is_q = hh < p.hq;
+    uint16_t* dst;
+    if (is_q) {
+      dst = p.q_out + (static_cast<size_t>(t) * p.hq + hh) * D;
+    } else {
       if (slot < 0) continue;
-      const int vh = hh - p.hq - p.hkv;
+      dst = p.k_pool + (hh - p.hq) * pool_head_stride + static_cast<size_t>(slot) * D;
+    }
+    if (!has) continue;
+    if (pos < 0) {  // inactive token: zero query output
+      *reinterpret_cast<uint32_t*>(dst + e) = 0u;
+      *reinterpret_cast<uint32_t*>(dst + H + e) = 0u;
+      continue;
+    }
+    const int set = is_q ? 0 : 1;
+    const bool normed = is_q ? norm_q : norm_k;
+    const DF r = normed ? s_r[hh] : DF{1.f, 0.f};
+    uint32_t lo_bits = 0, hi_bits = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = e + k;
+      const float x1 = k ? bf16_hi(xlo[j]) : bf16_lo(xlo[j]);
+      const float x2 = k ? bf16_hi(xhi[j]) : bf16_lo(xhi[j]);
+      DF o1 = dot2(x1, s_coef[set][0][i], x2, s_coef[set][1][i]);
+      const DF nd = {-s_coef[set][3][i].hi, -s_coef[set][3][i].lo};
+      DF o2 = dot2(x2, s_coef[set][2][i], x1, nd);
+      if (normed) {
+        o1 = mul_df(o1, r);
+        o2 = mul_df(o2, r);
+      }
+      lo_bits |= df_to_bf16(o1) << (16 * k);
+      hi_bits |= df_to_bf16(o2) << (16 * k);
+    }
+    *reinterpret_cast<uint32_t*>(dst + e) = lo_bits;
+    *reinterpret_cast<uint32_t*>(dst + H + e) = hi_bits;
+  }
+  // value heads: bit copy into the slot
+  if (slot >= 0) {
+    for (int vh = warp; vh < p.hkv; vh += kWarps) {
       const uint4* src = reinterpret_cast<const uint4*>(p.v + (static_cast<size_t>(t) * p.hkv + vh) * D);
       uint4* dst = reinterpret_cast<uint4*>(p.v_pool + vh * pool_head_stride + static_cast<size_t>(slot) * D);
       if (lane < D / 8) dst[lane] = src[lane];
-      continue;
     }
-    const bool is_q = hh < p.hq;
-    const int head = is_q ? hh : hh - p.hq;
-    uint16_t* dst;
-    if (is_q) {
-      dst = p.q_out + (static_cast<size_t>(t) * p.hq + head) * D;
-    } else {
-      if (slot < 0) continue;
-      dst = p.k_pool + head * pool_head_stride + static_cast<size_t>(slot) * D;
-    }
-    if (pos < 0) {  // inactive token: zero query output
-      if (has) {
-        st_u32(dst + e, 0u);
-        st_u32(dst + H + e, 0u);
-      }
-      continue;
-    }
-    const uint16_t* src =
-        is_q ? p.q + (static_cast<size_t>(t) * p.hq + head) * D : p.k + (static_cast<size_t>(t) * p.hkv + head) * D;
-    double x1a = 0.0, x1b = 0.0, x2a = 0.0, x2b = 0.0;
-    if (has) {
-      const uint32_t lo = ld_u32(src + e);
-      const uint32_t hi = ld_u32(src + H + e);
-      x1a = bf16_to_double(static_cast<uint16_t>(lo & 0xFFFFu));
-      x1b = bf16_to_double(static_cast<uint16_t>(lo >> 16));
-      x2a = bf16_to_double(static_cast<uint16_t>(hi & 0xFFFFu));
-      x2b = bf16_to_double(static_cast<uint16_t>(hi >> 16));
-    }
-    const uint16_t* w = is_q ? p.q_norm_w : p.k_norm_w;
-    if (w != nullptr) {
-      double ss = __dadd_rn(__dadd_rn(__dmul_rn(x1a, x1a), __dmul_rn(x1b, x1b)),
-                            __dadd_rn(__dmul_rn(x2a, x2a), __dmul_rn(x2b, x2b)));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-      const double r = 1.0 / sqrt(__dadd_rn(ss / static_cast<double>(D), p.norm_eps));
-      if (has) {
-        const uint32_t wlo = ld_u32(w + e);
-        const uint32_t whi = ld_u32(w + H + e);
-        x1a = __dmul_rn(__dmul_rn(x1a, r), bf16_to_double(static_cast<uint16_t>(wlo & 0xFFFFu)));
-        x1b = __dmul_rn(__dmul_rn(x1b, r), bf16_to_double(static_cast<uint16_t>(wlo >> 16)));
-        x2a = __dmul_rn(__dmul_rn(x2a, r), bf16_to_double(static_cast<uint16_t>(whi & 0xFFFFu)));
-        x2b = __dmul_rn(__dmul_rn(x2b, r), bf16_to_double(static_cast<uint16_t>(whi >> 16)));
-      }
-    }
-    if (!has) continue;
-    const double ca = s_cos[e], sa = s_sin[e], cb = s_cos[e + 1], sb = s_sin[e + 1];
-    const double o1a = __dsub_rn(__dmul_rn(x1a, ca), __dmul_rn(x2a, sa));
-    const double o2a = __dadd_rn(__dmul_rn(x2a, ca), __dmul_rn(x1a, sa));
-    const double o1b = __dsub_rn(__dmul_rn(x1b, cb), __dmul_rn(x2b, sb));
-    const double o2b = __dadd_rn(__dmul_rn(x2b, cb), __dmul_rn(x1b, sb));
-    st_u32(dst + e, static_cast<uint32_t>(double_to_bf16(o1a)) |
-                        (static_cast<uint32_t>(double_to_bf16(o1b)) << 16));
-    st_u32(dst + H + e, static_cast<uint32_t>(double_to_bf16(o2a)) |
-                            (static_cast<uint32_t>(double_to_bf16(o2b)) << 16));
   }
 }
 
@@ -180,10 +252,11 @@ __global__ void __launch_bounds__(256) append_rope_kernel(const AppendParams p) 
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
+  if (p.hq + p.hkv > kWarps * kMaxHeadsPerWarp) return cudaErrorInvalidValue;
   switch (head_dim) {
-    case 64: append_rope_kernel<64><<<p.T, 256, 0, stream>>>(p); break;
-    case 96: append_rope_kernel<96><<<p.T, 256, 0, stream>>>(p); break;
-    case 128: append_rope_kernel<128><<<p.T, 256, 0, stream>>>(p); break;
+    case 64: append_rope_kernel<64><<<p.T, kWarps * 32, 0, stream>>>(p); break;
+    case 96: append_rope_kernel<96><<<p.T, kWarps * 32, 0, stream>>>(p); break;
+    case 128: append_rope_kernel<128><<<p.T, kWarps * 32, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

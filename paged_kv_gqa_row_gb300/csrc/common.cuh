@@ -47,8 +47,7 @@ struct DecodeParams {
   const int32_t* table;       // [num_rows][pages_per_row]
   uint16_t* out;              // [B][Hq][D]
   int32_t* status;
-  int32_t* ws_meta;           // [0] = page-heads per CTA
-  int32_t* ws_pref;           // [B + 1] prefix sums of visible pages per row
+  int32_t* ws_count;          // [B][Hkv] finished segments of cut pairs (zero at rest)
   float* ws_ml;               // [segments][G][2]: running max (log2 units), sum
   float* ws_o;                // [segments][G][D]: unnormalised partial outputs
   int B, hq, hkv, group, num_pages, pages_per_row, window;
@@ -62,7 +61,7 @@ struct DecodeLaunch {
 
 // Workspace layout for `rows` decode rows and `grid` CTAs (byte offsets).
 struct DecodeWorkspace {
-  size_t meta, pref, ml, o, total;
+  size_t count, ml, o, total;
 };
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 

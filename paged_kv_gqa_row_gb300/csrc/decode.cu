@@ -1,37 +1,49 @@
-// K2 + K3: paged split-KV decode attention and its log-sum-exp combine.
+// K2 + K3: paged split-KV decode attention with a fused log-sum-exp combine.
 //
 // Work decomposition.  Decode row b at position p sees keys
 // [max(0, p - window + 1), p], i.e. np_b pages of 64 (the first and last may
 // be partial).  Each (row, kv head) pair is a run of np_b page-heads; the runs
 // of all pairs, (b, h) with h fastest, are laid end to end and the resulting
 // stream of page-heads is cut into gridDim.x equal pieces, one per persistent
-// CTA.  A pair that falls inside one CTA is finished there (output written
-// directly); a pair cut by CTA boundaries leaves one partial result per CTA
-// (unnormalised output, running max, running sum) and the combine kernel
-// merges them.  Pair q = b * Hkv + h touching CTA c writes segment q + c,
-// which is unique because consecutive pairs never go back to an earlier CTA.
+// CTA, so every CTA moves the same number of pages whatever the length mix.
+// The part of a pair inside one CTA is a segment.  A pair that falls inside
+// one CTA is finished there (output written directly).  A pair cut by CTA
+// boundaries leaves one partial result per CTA (unnormalised output, running
+// max, running sum; pair q on CTA c writes segment q + c, unique because
+// consecutive pairs never go back to an earlier CTA); each such CTA then
+// increments the pair's counter, and the last one to arrive merges the
+// partials and writes the output (the counter returns to zero).  A CTA
+// processes the segment it shares with the next CTA first, so that cut pairs
+// finish early instead of in the tail.
 //
-// CTA structure (160 threads).  Warp 4 is the producer: one lane walks the
-// CTA's page-heads, reads the page table, and loads each page's K and V
-// (64 positions x head_dim bf16, contiguous in the head-major pool) with 2-D
-// TMA tile copies into a ring of shared-memory stages (128-byte swizzle),
-// completing on the stage's "full" mbarrier.  Warps 0-3 consume every stage:
-// warp w owns keys 16w .. 16w + 15 of the page and keeps its own online
-// softmax state.  Per page and warp:
-//   S^T[16 keys, 8 heads] = K[16 keys, D] * Q^T  (mma m16n8k16, keys as M,
-//                                                  the GQA group padded to N = 8)
-//   O^T[D, 8 heads]      += V^T[D, 16 keys] * P^T (V^T via ldmatrix.trans,
-//                                                  P^T via movmatrix.trans of
-//                                                  the S fragment)
-// At the end of a pair's run inside the CTA the four warps merge through
-// shared memory.
+// CTA structure (192 threads, warp-specialised):
+//  * warp 4, producer: one lane walks the CTA's page-heads, reads the page
+//    table, and loads each page's K and V (64 positions x head_dim bf16,
+//    contiguous in the head-major pool) with 2-D TMA tile copies into a ring
+//    of shared-memory stages (128-byte swizzle), plus the segment's G query
+//    rows (one 1-D bulk copy) on a segment's first page; all complete on the
+//    stage's "full" mbarrier.
+//  * warps 0-3, consumers: warp w owns keys 16w .. 16w + 15 of every page.
+//    It copies its K and V fragments to registers (ldmatrix), releases the
+//    stage at once, and then computes
+//      S^T[16 keys, 8 heads] = K[16 keys, D] Q^T   (mma m16n8k16, keys as M,
+//                                                   the GQA group padded to N)
+//      O^T[D, 8 heads]      += V^T[D, 16 keys] P^T (P^T via movmatrix.trans
+//                                                   of the S fragment)
+//    with an online softmax in the log2 domain.  At a segment's end each warp
+//    hands its state to the epilogue through one of two staging slots.
+//  * warp 5, epilogue: merges the four warps' states of each segment and
+//    writes the output (whole pairs) or the partial, counter and, for the
+//    last arriver, the merged output of a cut pair.  Consumers never wait on
+//    global memory.
+// The per-row prologue (visible pages, prefix sums) reads only positions, so
+// it overlaps the previous kernel on the stream (programmatic dependent
+// launch); the kernel waits for that kernel before touching q or the pool.
 //
 // Sources: "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
 // (decode_rows: a row attends over itself up to its position; window_mask;
 // scale rsqrt(head_dim)); "Mistral 7B Instruct v0.3", Entries table
 // (decode_paged: the pool, pages of 64, table[b]).
-#include <cfloat>
-
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -39,28 +51,39 @@ namespace lnk {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
-constexpr int kPairFirst = 1;
-constexpr int kPairLast = 2;
+constexpr int kProducerWarp = 4;
+constexpr int kEpilogueWarp = 5;
+constexpr int kThreads = 6 * 32;
+#ifndef LNK_DECODE_STAGES
+#define LNK_DECODE_STAGES 4
+#endif
+constexpr int kStages = LNK_DECODE_STAGES;  // K+V pages in flight per CTA
+constexpr int kSegFirst = 1;
+constexpr int kSegLast = 2;
 constexpr int kPairWhole = 4;
+constexpr int kCtaLast = 8;
 
 struct StageInfo {
-  int b, h, klo, khi, flags, seg;
+  int b, h, klo, khi, flags, seg, nseg, c0;
 };
 
 template <int D>
 struct DecodeSmem {
   static constexpr int NB = boxes_for(D);
-  static constexpr int kStageBytes = 2 * NB * kBoxBytes;          // K boxes, then V boxes
-  static constexpr int kOStride = D + 4;                          // padded staging row
+  static constexpr int kStageBytes = 2 * NB * kBoxBytes;  // K boxes, then V boxes
+  static constexpr int kQBytes = kMaxGroup * D * 2;       // query rows of the stage's segment
+  static constexpr int kOStride = D + 4;                  // padded staging row
+  static constexpr int kSlotFloats = kConsumerWarps * kMaxGroup * kOStride;
   static constexpr size_t stages = 0;
-  static constexpr size_t bars = stages + size_t(kStages) * kStageBytes;
-  static constexpr size_t info = bars + (2 * kStages + 2) * sizeof(uint64_t);
-  static constexpr size_t ostage = info + kStages * sizeof(StageInfo);
-  static constexpr size_t mstage = ostage + size_t(kConsumerWarps) * kMaxGroup * kOStride * 4;
-  static constexpr size_t lstage = mstage + kConsumerWarps * kMaxGroup * 4;
-  static constexpr size_t misc = lstage + kConsumerWarps * kMaxGroup * 4;  // abort flag, totals
+  static constexpr size_t qbuf = stages + size_t(kStages) * kStageBytes;
+  static constexpr size_t bars = qbuf + size_t(kStages) * kQBytes;
+  static constexpr size_t info = bars + (2 * kStages + 4) * sizeof(uint64_t);
+  static constexpr size_t slot_info = info + kStages * sizeof(StageInfo);
+  static constexpr size_t ostage = slot_info + 2 * sizeof(StageInfo);
+  static constexpr size_t mstage = ostage + 2 * size_t(kSlotFloats) * 4;
+  static constexpr size_t lstage = mstage + 2 * kConsumerWarps * kMaxGroup * 4;
+  static constexpr size_t epi = lstage + 2 * kConsumerWarps * kMaxGroup * 4;   // epilogue scratch
+  static constexpr size_t misc = epi + 2 * kMaxGroup * 4;                       // abort flag, scan sums
   static constexpr size_t pref = misc + 64;
   static size_t bytes(int B) { return pref + size_t(B + 1) * 4 + 1024; }  // + alignment slack
 };
@@ -75,6 +98,38 @@ __device__ __forceinline__ int visible_pages(int pos, int window, int pages_per_
   return pos / kPage - lo / kPage + 1;
 }
 
+// Where page-head `gi` of the flattened stream lies, and the per-pair values
+// the producer needs (computed once per pair, not per page).
+struct Cursor {
+  int b, h, j, np, pos, lo, first_page;
+  int seg, c0, nseg, whole;
+  const int* trow;
+};
+
+__device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref, const DecodeParams& p,
+                                       long long start, long long end, long long per) {
+  int lo_b = 0, hi_b = p.B - 1;  // largest b with hkv * pref[b] <= gi
+  while (lo_b < hi_b) {
+    const int mid = (lo_b + hi_b + 1) >> 1;
+    if (static_cast<long long>(pref[mid]) * p.hkv <= gi) lo_b = mid; else hi_b = mid - 1;
+  }
+  c.b = lo_b;
+  c.np = pref[c.b + 1] - pref[c.b];
+  const long long rem = gi - static_cast<long long>(pref[c.b]) * p.hkv;
+  c.h = static_cast<int>(rem / c.np);
+  c.j = static_cast<int>(rem % c.np);
+  c.pos = p.positions[c.b];
+  c.lo = p.window > 0 ? max(0, c.pos - p.window + 1) : 0;
+  c.first_page = c.lo / kPage;
+  c.trow = p.table + static_cast<long long>(c.b) * p.pages_per_row;
+  const long long pair_start = gi - c.j;
+  const long long pair_end = pair_start + c.np;
+  c.whole = pair_start >= start && pair_end <= end;
+  c.c0 = static_cast<int>(pair_start / per);
+  c.nseg = static_cast<int>((pair_end - 1) / per) - c.c0 + 1;
+  c.seg = c.b * p.hkv + c.h + static_cast<int>(blockIdx.x);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -86,31 +141,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* merge_bar = empty_bar + kStages;  // [0]: staging written, [1]: staging read
+  uint64_t* slot_full = empty_bar + kStages;  // [2]: consumer warps -> epilogue
+  uint64_t* slot_empty = slot_full + 2;       // [2]: epilogue -> consumer warps
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::info);
+  StageInfo* slot_info = reinterpret_cast<StageInfo*>(smem + L::slot_info);
   float* ost = reinterpret_cast<float*>(smem + L::ostage);
   float* mst = reinterpret_cast<float*>(smem + L::mstage);
   float* lst = reinterpret_cast<float*>(smem + L::lstage);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc);
-  int* scan_tot = reinterpret_cast<int*>(smem + L::ostage);  // reuses the staging area at start
+  int* misc = reinterpret_cast<int*>(smem + L::misc);  // [0] abort, [2..7] warp sums of the scan
+  volatile int* abort_flag = misc;
   int* pref = reinterpret_cast<int*>(smem + L::pref);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int B = p.B;
+  const int G = p.group;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(full_bar + s), 1);
       mbar_init(smem_addr(empty_bar + s), kConsumerWarps);
     }
-    mbar_init(smem_addr(merge_bar + 0), kConsumerWarps * 32);
-    mbar_init(smem_addr(merge_bar + 1), kConsumerWarps * 32);
-    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(slot_full + i), kConsumerWarps);
+      mbar_init(smem_addr(slot_empty + i), 1);
+    }
+    misc[0] = 0;
     fence_mbarrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_descriptor(&kmap);
     tma_prefetch_descriptor(&vmap);
   }
@@ -125,20 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       pref[b + 1] = run;
     }
     if (bad && p.status != nullptr && blockIdx.x == 0) atomicOr(p.status, bad);
-    scan_tot[tid] = run;
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0;
-      for (int i = 0; i < kThreads; ++i) {
-        const int v = scan_tot[i];
-        scan_tot[i] = acc;
-        acc += v;
-      }
-      pref[0] = 0;
+    int incl = run;  // inclusive scan of the per-thread totals across the block
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
+    if (lane == 31) misc[2 + warp] = incl;
     __syncthreads();
-    const int off = scan_tot[tid];
+    int off = incl - run;
+    for (int w = 0; w < warp; ++w) off += misc[2 + w];
     for (int b = r0; b < r1; ++b) pref[b + 1] += off;
+    if (tid == 0) pref[0] = 0;
     __syncthreads();
   }
 
@@ -146,94 +204,234 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long per = (total + gridDim.x - 1) / gridDim.x;
   const long long start = min(total, static_cast<long long>(blockIdx.x) * per);
   const long long end = min(total, start + per);
-  if (blockIdx.x == 0) {
-    if (tid == 0) p.ws_meta[0] = static_cast<int>(per);
-    for (int b = tid; b <= B; b += kThreads) p.ws_pref[b] = pref[b];
+
+  // Wait for the previous kernel on the stream (it writes q and the pool).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // rows with nothing to attend to get a zero output
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (pref[b + 1] == pref[b]) {
+      uint32_t* o = reinterpret_cast<uint32_t*>(p.out + static_cast<size_t>(b) * p.hq * D);
+      for (int i = tid; i < p.hq * D / 2; i += kThreads) o[i] = 0u;
+    }
   }
   if (start >= end) return;
+  const int nsteps = static_cast<int>(end - start);
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ============================== producer ==============================
     if (lane != 0) return;
-    // locate the pair holding page-head `start`
-    int lo_b = 0, hi_b = B - 1;  // largest b with hkv * pref[b] <= start
-    while (lo_b < hi_b) {
-      const int mid = (lo_b + hi_b + 1) >> 1;
-      if (static_cast<long long>(pref[mid]) * p.hkv <= start) lo_b = mid; else hi_b = mid - 1;
+    // Order: the CTA's last segment first when its pair continues into the
+    // next CTA, then everything else in stream order.
+    Cursor cur;
+    locate(cur, end - 1, pref, p, start, end, per);
+    const long long last_seg = max(start, end - 1 - cur.j);
+    const bool last_cut = (end - 1 - cur.j) + cur.np > end;
+    long long r_begin[2], r_end[2];
+    int nranges = 1;
+    if (last_cut && last_seg > start) {
+      r_begin[0] = last_seg; r_end[0] = end;
+      r_begin[1] = start;    r_end[1] = last_seg;
+      nranges = 2;
+    } else {
+      r_begin[0] = start; r_end[0] = end;
     }
-    int b = lo_b;
-    int np = pref[b + 1] - pref[b];
-    long long rem = start - static_cast<long long>(pref[b]) * p.hkv;
-    int h = static_cast<int>(rem / np);
-    int j = static_cast<int>(rem % np);
-    int pos = p.positions[b];
-    int lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
-    int first_page = lo / kPage;
-    const int* trow = p.table + static_cast<long long>(b) * p.pages_per_row;
-
+    const uint32_t q_bytes = static_cast<uint32_t>(G * D * 2);
     int k = 0;
-    for (long long gi = start; gi < end; ++gi, ++k) {
-      const int s = k % kStages;
-      if (k >= kStages) {
-        if (!mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) break;
-      }
-      const int lp = first_page + j;
-      const int page = trow[lp];
-      StageInfo si;
-      si.b = b;
-      si.h = h;
-      si.klo = max(lo - lp * kPage, 0);
-      si.khi = min(pos - lp * kPage + 1, kPage);
-      const long long pair_start = gi - j;
-      si.flags = ((gi == start || j == 0) ? kPairFirst : 0) | ((gi == end - 1 || j == np - 1) ? kPairLast : 0) |
-                 ((pair_start >= start && pair_start + np <= end) ? kPairWhole : 0);
-      si.seg = b * p.hkv + h + static_cast<int>(blockIdx.x);
-      const uint32_t fb = smem_addr(full_bar + s);
-      if (page < 0 || page >= p.num_pages) {
-        if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
-        si.klo = si.khi = 0;
-        info[s] = si;
-        mbar_arrive(fb);
-      } else {
-        info[s] = si;
-        mbar_arrive_expect_tx(fb, L::kStageBytes);
-        const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
-        const uint32_t vdst = kdst + NB * kBoxBytes;
-        const int y = (h * p.num_pages + page) * kPage;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
-          tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
+    bool stop = false;
+    for (int rg = 0; rg < nranges && !stop; ++rg) {
+      locate(cur, r_begin[rg], pref, p, start, end, per);
+      for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
+        const int s = k % kStages;
+        if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
+          stop = true;
+          break;
         }
-      }
-      // advance to the next page-head
-      if (++j == np) {
-        j = 0;
-        if (++h == p.hkv) {
-          h = 0;
-          do { ++b; } while (b < B && pref[b + 1] == pref[b]);
-          if (b < B) {
-            np = pref[b + 1] - pref[b];
-            pos = p.positions[b];
-            lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
-            first_page = lo / kPage;
-            trow = p.table + static_cast<long long>(b) * p.pages_per_row;
+        const int lp = cur.first_page + cur.j;
+        const int page = cur.trow[lp];
+        StageInfo si;
+        si.b = cur.b;
+        si.h = cur.h;
+        si.klo = max(cur.lo - lp * kPage, 0);
+        si.khi = min(cur.pos - lp * kPage + 1, kPage);
+        const bool first = gi == r_begin[rg] || cur.j == 0;
+        si.flags = (first ? kSegFirst : 0) | ((gi == r_end[rg] - 1 || cur.j == cur.np - 1) ? kSegLast : 0) |
+                   (cur.whole ? kPairWhole : 0) | (k == nsteps - 1 ? kCtaLast : 0);
+        si.seg = cur.seg;
+        si.nseg = cur.nseg;
+        si.c0 = cur.c0;
+        const bool valid = page >= 0 && page < p.num_pages;
+        if (!valid) {
+          if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
+          si.klo = si.khi = 0;
+        }
+        info[s] = si;
+        const uint32_t fb = smem_addr(full_bar + s);
+        const uint32_t tx = (valid ? static_cast<uint32_t>(L::kStageBytes) : 0u) + (first ? q_bytes : 0u);
+        if (tx) mbar_arrive_expect_tx(fb, tx); else mbar_arrive(fb);
+        if (first) {
+          const uint16_t* qsrc = p.q + (static_cast<size_t>(cur.b) * p.hq + static_cast<size_t>(cur.h) * G) * D;
+          bulk_load(smem_addr(smem + L::qbuf + size_t(s) * L::kQBytes), qsrc, q_bytes, fb);
+        }
+        if (valid) {
+          const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+          const uint32_t vdst = kdst + NB * kBoxBytes;
+          const int y = (cur.h * p.num_pages + page) * kPage;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
+            tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
           }
         }
+        // advance to the next page-head
+        if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per);
       }
     }
     // Drain: do not leave the CTA while a copy may still land in its memory.
     const int issued = k;
     for (int kk = max(0, issued - kStages); kk < issued; ++kk) {
-      const int s = kk % kStages;
-      const uint32_t fb = smem_addr(full_bar + s);
-      if (!mbar_try_wait(fb, (kk / kStages) & 1)) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(fb, (kk / kStages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {
-        }
+      const uint32_t fb = smem_addr(full_bar + kk % kStages);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(fb, (kk / kStages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {
       }
     }
     if (*abort_flag && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
+    return;
+  }
+
+  if (warp == kEpilogueWarp) {
+    // ============================== epilogue ==============================
+    float* eml = reinterpret_cast<float*>(smem + L::epi);  // [2][kMaxGroup]: max, sum per head
+    constexpr int D4 = D / 4;
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      if (!mbar_wait(smem_addr(slot_full + slot), (n >> 1) & 1, abort_flag)) break;
+      const StageInfo si = slot_info[slot];
+      const float* os = ost + size_t(slot) * L::kSlotFloats;
+      const float* ms = mst + slot * kConsumerWarps * kMaxGroup;
+      const float* ls = lst + slot * kConsumerWarps * kMaxGroup;
+      const bool whole = (si.flags & kPairWhole) != 0;
+      uint16_t* out_pair = p.out + (static_cast<size_t>(si.b) * p.hq + static_cast<size_t>(si.h) * G) * D;
+      const int q = si.b * p.hkv + si.h;
+      // per head: merged max and sum of the four warps
+      if (lane < G) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ms[w * kMaxGroup + lane]);
+        float Ls = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = ms[w * kMaxGroup + lane];
+            if (mw != -INFINITY) Ls += ls[w * kMaxGroup + lane] * exp2f(mw - M);
+          }
+        }
+        eml[lane] = M;
+        eml[kMaxGroup + lane] = Ls;
+      }
+      __syncwarp();
+      for (int it = lane; it < G * D4; it += 32) {
+        const int g = it / D4, d = (it % D4) * 4;
+        const float M = eml[g], Ls = eml[kMaxGroup + g];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = ms[w * kMaxGroup + g];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            const float4 v = *reinterpret_cast<const float4*>(os + (w * kMaxGroup + g) * L::kOStride + d);
+            acc.x += v.x * f;
+            acc.y += v.y * f;
+            acc.z += v.z * f;
+            acc.w += v.w * f;
+          }
+        }
+        if (whole) {
+          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          uint2 pk;
+          pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(out_pair + g * D + d) = pk;
+        } else {
+          *reinterpret_cast<float4*>(p.ws_o + (static_cast<size_t>(si.seg) * G + g) * D + d) = acc;
+          if (d == 0) {
+            p.ws_ml[(static_cast<size_t>(si.seg) * G + g) * 2 + 0] = M;
+            p.ws_ml[(static_cast<size_t>(si.seg) * G + g) * 2 + 1] = Ls;
+          }
+        }
+      }
+      __syncwarp();
+      // staging slot consumed
+      if (lane == 0) mbar_arrive(smem_addr(slot_empty + slot));
+      if (!whole) {
+        // publish the partial, then count the pair's finished segments
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int old = atomicAdd(p.ws_count + q, 1);
+          last = old == si.nseg - 1;
+          if (last) p.ws_count[q] = 0;  // ready for the next call
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const size_t seg0 = static_cast<size_t>(q + si.c0);
+          const int nsg = si.nseg;
+          // pass 1: per head, online max/sum over the pair's segments; lane
+          // handles head lane % G of segments lane / G, lane / G + 32 / G, ...
+          float rm = -INFINITY, rl = 0.f;
+          for (int i = lane; i < nsg * G; i += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + seg0 * G + i);
+            if (ml.x != -INFINITY) {
+              const float mn = fmaxf(rm, ml.x);
+              rl = rl * exp2f(rm - mn) + ml.y * exp2f(ml.x - mn);
+              rm = mn;
+            }
+          }
+          for (int off = G; off < 32; off <<= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, rm, off);
+            const float ol = __shfl_xor_sync(0xffffffffu, rl, off);
+            const float mn = fmaxf(rm, om);
+            if (mn != -INFINITY) {
+              rl = (rm == -INFINITY ? 0.f : rl * exp2f(rm - mn)) + (om == -INFINITY ? 0.f : ol * exp2f(om - mn));
+              rm = mn;
+            }
+          }
+          __syncwarp();
+          if (lane < G) {
+            eml[lane] = rm;
+            eml[kMaxGroup + lane] = rl;
+          }
+          __syncwarp();
+          // pass 2: weighted sum of the partial outputs (independent loads)
+          for (int it = lane; it < G * D4; it += 32) {
+            const int g = it / D4, d = (it % D4) * 4;
+            const float M = eml[g], Ls = eml[kMaxGroup + g];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
+              for (int sg = 0; sg < nsg; ++sg) {
+                const size_t row = (seg0 + sg) * G + g;
+                const float mseg = __ldcg(p.ws_ml + row * 2);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + row * D + d));
+                const float f = mseg == -INFINITY ? 0.f : exp2f(mseg - M);
+                acc.x += v.x * f;
+                acc.y += v.y * f;
+                acc.z += v.z * f;
+                acc.w += v.w * f;
+              }
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(out_pair + g * D + d) = pk;
+          }
+        }
+      }
+      if (si.flags & kCtaLast) break;
+    }
+    if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
     return;
   }
 
@@ -246,27 +444,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t qf[DK][2];
   float o[DK][4];
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  uint32_t merges = 0;
+  int nseg_done = 0;
 
-  const int nsteps = static_cast<int>(end - start);
   for (int k = 0; k < nsteps; ++k) {
     const int s = k % kStages;
     if (!mbar_wait(smem_addr(full_bar + s), (k / kStages) & 1, abort_flag)) break;
     const StageInfo si = info[s];
-    if (si.flags & kPairFirst) {
-      const uint16_t* qrow = p.q + (static_cast<size_t>(si.b) * p.hq + static_cast<size_t>(si.h) * p.group) * D;
-      const bool gv = r < p.group;
+    if (si.flags & kSegFirst) {
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + L::qbuf + size_t(s) * L::kQBytes);
+      const bool gv = r < G;
 #pragma unroll
       for (int kk = 0; kk < DK; ++kk) {
-        qf[kk][0] = gv ? *reinterpret_cast<const uint32_t*>(qrow + r * D + kk * 16 + 2 * c) : 0u;
-        qf[kk][1] = gv ? *reinterpret_cast<const uint32_t*>(qrow + r * D + kk * 16 + 8 + 2 * c) : 0u;
+        qf[kk][0] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 2 * c) : 0u;
+        qf[kk][1] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 8 + 2 * c) : 0u;
       }
 #pragma unroll
       for (int dt = 0; dt < DK; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
       m_a = m_b = -INFINITY;
       l_a = l_b = 0.f;
     }
-    if (si.khi > si.klo && si.klo < key0 + 16 && si.khi > key0) {
+    const bool work = si.khi > si.klo && si.klo < key0 + 16 && si.khi > key0;
+    uint32_t ka[DK][4], va[DK][4];
+    if (work) {
       const uint8_t* kbuf = stage_base + size_t(s) * L::kStageBytes;
       const uint8_t* vbuf = kbuf + NB * kBoxBytes;
       if (si.klo > key0 || si.khi < key0 + 16) {
@@ -286,26 +485,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t kaddr = smem_addr(kbuf);
       const uint32_t vaddr = smem_addr(vbuf);
-      // ---- S^T = K Q^T ----
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int key = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int kkey = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int vkey = key0 + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-        for (int kk = 0; kk < DK; ++kk) {
-          const int chunk = kk * 2 + (lane >> 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kaddr + (chunk >> 3) * kBoxBytes + swz128(key, chunk & 7), a0, a1, a2, a3);
-          mma_bf16_16816(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-        }
+      for (int kk = 0; kk < DK; ++kk) {
+        const int chunk = kk * 2 + (lane >> 4);
+        ldsm_x4(kaddr + (chunk >> 3) * kBoxBytes + swz128(kkey, chunk & 7), ka[kk][0], ka[kk][1], ka[kk][2],
+                ka[kk][3]);
+      }
+#pragma unroll
+      for (int dt = 0; dt < DK; ++dt) {
+        const int chunk = dt * 2 + ((lane >> 3) & 1);
+        ldsm_x4_trans(vaddr + (chunk >> 3) * kBoxBytes + swz128(vkey, chunk & 7), va[dt][0], va[dt][1],
+                      va[dt][2], va[dt][3]);
+      }
+    }
+    // the fragments are in registers: release the stage before the math
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(empty_bar + s));
+
+    if (work) {
+      // ---- S^T = K Q^T (two independent accumulation chains) ----
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < DK; kk += 2) {
+        mma_bf16_16816(sc, ka[kk][0], ka[kk][1], ka[kk][2], ka[kk][3], qf[kk][0], qf[kk][1]);
+        if (kk + 1 < DK)
+          mma_bf16_16816(sd, ka[kk + 1][0], ka[kk + 1][1], ka[kk + 1][2], ka[kk + 1][3], qf[kk + 1][0],
+                         qf[kk + 1][1]);
       }
       // ---- mask, online softmax (log2 domain) ----
       const int kr0 = key0 + r, kr1 = kr0 + 8;
       const bool v0 = kr0 >= si.klo && kr0 < si.khi;
       const bool v1 = kr1 >= si.klo && kr1 < si.khi;
-      const float s0 = v0 ? sc[0] * p.scale_log2 : -INFINITY;
-      const float s1 = v0 ? sc[1] * p.scale_log2 : -INFINITY;
-      const float s2 = v1 ? sc[2] * p.scale_log2 : -INFINITY;
-      const float s3 = v1 ? sc[3] * p.scale_log2 : -INFINITY;
+      const float s0 = v0 ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
+      const float s1 = v0 ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
+      const float s2 = v1 ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
+      const float s3 = v1 ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
       float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -322,45 +538,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_b = l_b * al_b + (p1 + p3);
       m_a = mn_a;
       m_b = mn_b;
+      // ---- O^T = O^T * alpha + V^T P^T ----
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
 #pragma unroll
       for (int dt = 0; dt < DK; ++dt) {
         o[dt][0] *= al_a;
         o[dt][1] *= al_b;
         o[dt][2] *= al_a;
         o[dt][3] *= al_b;
-      }
-      // ---- O^T += V^T P^T ----
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-      {
-        const int key = key0 + (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-        for (int dt = 0; dt < DK; ++dt) {
-          const int chunk = dt * 2 + ((lane >> 3) & 1);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(vaddr + (chunk >> 3) * kBoxBytes + swz128(key, chunk & 7), a0, a1, a2, a3);
-          mma_bf16_16816(o[dt], a0, a1, a2, a3, pb0, pb1);
-        }
+        mma_bf16_16816(o[dt], va[dt][0], va[dt][1], va[dt][2], va[dt][3], pb0, pb1);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(empty_bar + s));
 
-    if (si.flags & kPairLast) {
-      // ---- merge the four warps' states for this pair ----
+    if (si.flags & kSegLast) {
+      // ---- hand this warp's state for the segment to the epilogue ----
       float la = l_a, lb = l_b;
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         la += __shfl_xor_sync(0xffffffffu, la, off);
         lb += __shfl_xor_sync(0xffffffffu, lb, off);
       }
+      const int slot = nseg_done & 1;
+      if (!mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag)) break;
       if (lane < 4) {
-        mst[warp * kMaxGroup + 2 * c] = m_a;
-        mst[warp * kMaxGroup + 2 * c + 1] = m_b;
-        lst[warp * kMaxGroup + 2 * c] = la;
-        lst[warp * kMaxGroup + 2 * c + 1] = lb;
+        mst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c] = m_a;
+        mst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c + 1] = m_b;
+        lst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c] = la;
+        lst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c + 1] = lb;
       }
-      float* ow = ost + size_t(warp) * kMaxGroup * L::kOStride;
+      if (warp == 0 && lane == 0) slot_info[slot] = si;
+      float* ow = ost + size_t(slot) * L::kSlotFloats + size_t(warp) * kMaxGroup * L::kOStride;
 #pragma unroll
       for (int dt = 0; dt < DK; ++dt) {
         ow[(2 * c) * L::kOStride + dt * 16 + r] = o[dt][0];
@@ -368,93 +576,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ow[(2 * c) * L::kOStride + dt * 16 + r + 8] = o[dt][2];
         ow[(2 * c + 1) * L::kOStride + dt * 16 + r + 8] = o[dt][3];
       }
-      mbar_arrive(smem_addr(merge_bar + 0));
-      if (!mbar_wait(smem_addr(merge_bar + 0), merges & 1, abort_flag)) break;
-      const int G = p.group;
-      const bool whole = (si.flags & kPairWhole) != 0;
-      for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-        const int g = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mst[w * kMaxGroup + g]);
-        float Lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = mst[w * kMaxGroup + g];
-            if (mw != -INFINITY) {
-              const float f = exp2f(mw - M);
-              Lsum += lst[w * kMaxGroup + g] * f;
-              acc += ost[(size_t(w) * kMaxGroup + g) * L::kOStride + d] * f;
-            }
-          }
-        }
-        if (whole) {
-          const float val = Lsum > 0.f ? acc / Lsum : 0.f;
-          p.out[(static_cast<size_t>(si.b) * p.hq + static_cast<size_t>(si.h) * G + g) * D + d] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(val));
-        } else {
-          p.ws_o[(static_cast<size_t>(si.seg) * G + g) * D + d] = acc;
-          if (d == 0) {
-            p.ws_ml[(static_cast<size_t>(si.seg) * G + g) * 2 + 0] = M;
-            p.ws_ml[(static_cast<size_t>(si.seg) * G + g) * 2 + 1] = Lsum;
-          }
-        }
-      }
-      mbar_arrive(smem_addr(merge_bar + 1));
-      if (!mbar_wait(smem_addr(merge_bar + 1), merges & 1, abort_flag)) break;
-      ++merges;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(slot_full + slot));
+      ++nseg_done;
     }
   }
   if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
 }
 
-// Merges the partial results of (row, kv head) pairs that were cut by CTA
-// boundaries, and zeroes the outputs of rows with no visible keys.
-template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
-  const int q = blockIdx.x;
-  const int b = q / p.hkv, h = q % p.hkv;
-  const int G = p.group;
-  const int np = p.ws_pref[b + 1] - p.ws_pref[b];
-  uint16_t* out = p.out + (static_cast<size_t>(b) * p.hq + static_cast<size_t>(h) * G) * D;
-  if (np == 0) {
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) out[idx] = 0;
-    return;
-  }
-  const long long per = p.ws_meta[0];
-  const long long start = static_cast<long long>(p.ws_pref[b]) * p.hkv + static_cast<long long>(h) * np;
-  const long long end = start + np;
-  const int c0 = static_cast<int>(start / per), c1 = static_cast<int>((end - 1) / per);
-  if (c0 == c1) return;  // finished inside one CTA
-  const int seg0 = q + c0, nseg = c1 - c0 + 1;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D, d = idx % D;
-    float M = -INFINITY;
-    for (int s = 0; s < nseg; ++s) M = fmaxf(M, p.ws_ml[(static_cast<size_t>(seg0 + s) * G + g) * 2]);
-    float Lsum = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < nseg; ++s) {
-        const size_t si = static_cast<size_t>(seg0 + s) * G + g;
-        const float ms = p.ws_ml[si * 2];
-        if (ms == -INFINITY) continue;
-        const float f = exp2f(ms - M);
-        Lsum += p.ws_ml[si * 2 + 1] * f;
-        acc += p.ws_o[si * D + d] * f;
-      }
-    }
-    out[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(Lsum > 0.f ? acc / Lsum : 0.f));
-  }
-}
-
 template <int D>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             const DecodeLaunch& launch, cudaStream_t stream) {
-  decode_kernel<D><<<launch.grid, kThreads, launch.smem_bytes, stream>>>(kmap, vmap, p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  combine_kernel<D><<<p.B * p.hkv, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(launch.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = launch.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D>, kmap, vmap, p);
 }
 
 template <int D>
@@ -474,9 +617,8 @@ DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_d
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   DecodeWorkspace w;
   const size_t segs = static_cast<size_t>(rows) * hkv + static_cast<size_t>(grid);
-  w.meta = 0;
-  w.pref = up(w.meta + 64);
-  w.ml = up(w.pref + (static_cast<size_t>(rows) + 1) * 4);
+  w.count = 0;
+  w.ml = up(w.count + static_cast<size_t>(rows) * hkv * 4);
   w.o = up(w.ml + segs * group * 2 * 4);
   w.total = up(w.o + segs * group * static_cast<size_t>(head_dim) * 4);
   return w;

@@ -73,7 +73,7 @@ class DeviceStep:
                                   w.pages_per_row, window=w.window)
         self.rope = lnk.rope_desc(w.theta, w.llama3)
         self.ws_bytes = max(lnk.lnk_paged_workspace_size(self.desc, max(w.B, 1)), 256)
-        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
         self.dec_positions = _i32(w.dec_positions, device)
         if w.P:
             self.ch_rows = _i32(w.ch_rows, device)
