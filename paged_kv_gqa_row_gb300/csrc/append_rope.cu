@@ -7,8 +7,9 @@
 // where c_i, s_i are the cosine and sine of the float32 angle
 // f32(position) * inv_freq[i], g the QK-norm weights and r the head's RMS
 // factor 1 / sqrt(mean(x^2) + eps) (g = r = 1 without QK-norm).  The four
-// per-frequency coefficients are evaluated once per token in double precision
-// and kept as pairs of floats (hi + lo); each element is then computed with
+// per-frequency coefficients are evaluated once per token as pairs of floats
+// (hi + lo; sine and cosine by a float-pair Taylor series after an exact
+// reduction by pi/2); each element is then computed with
 // error-free float products and sums (about 2^-46 relative error) and rounded
 // once to bf16, looking at the low part only to break an exact tie of the high
 // part.  The result is the correctly rounded value of the exact expression
@@ -65,6 +66,103 @@ __device__ __forceinline__ DF mul_df(DF a, DF r) {
   return two_sum(m.hi, l);
 }
 
+// |a| >= |b| (or a == 0): s + e == a + b exactly.
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  const DF t = two_sum(a.lo, b.lo);
+  const DF u = fast_two_sum(s.hi, __fadd_rn(s.lo, t.hi));
+  return fast_two_sum(u.hi, __fadd_rn(u.lo, t.lo));
+}
+
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const DF p = two_prod(a.hi, b.hi);
+  return fast_two_sum(p.hi, __fadd_rn(p.lo, __fmaf_rn(a.hi, b.lo, __fmul_rn(a.lo, b.hi))));
+}
+
+// a (bf16-exact) times a pair of floats
+__device__ __forceinline__ DF df_scale(float a, DF b) {
+  const DF p = two_prod(a, b.hi);
+  return fast_two_sum(p.hi, __fmaf_rn(a, b.lo, p.lo));
+}
+
+// 1 / n! as a pair of floats (evaluated in double, exact factorials up to 18!)
+struct Coef {
+  float hi, lo;
+};
+constexpr double inv_factorial(int n) {
+  double f = 1.0;
+  for (int i = 2; i <= n; ++i) f *= i;
+  return 1.0 / f;
+}
+constexpr Coef coef(int n, bool negative) {
+  const double v = negative ? -inv_factorial(n) : inv_factorial(n);
+  return {static_cast<float>(v), static_cast<float>(v - static_cast<double>(static_cast<float>(v)))};
+}
+
+// pi / 2 as the sum of three floats (to about 2^-76), from the digits of pi
+constexpr float kPio2a = 0x1.921fb6p+0f;
+constexpr float kPio2b = -0x1.777a5cp-25f;
+constexpr float kPio2c = -0x1.ee59dap-50f;
+constexpr float kTwoOverPi = 0x1.45f306p-1f;
+
+// sin and cos of a float angle (|a| < 2^20) as pairs of floats, to about
+// 2^-48 absolute: Cody-Waite reduction by pi/2 with error-free products
+// (k < 2^20 * 2/pi is an exact float integer), then the Taylor series of
+// sin and cos on |r| <= pi/4 (terms to r^17 and r^18) by Horner's rule, the
+// small high-order part in float and the rest in float pairs.
+__device__ __forceinline__ void sincos_df(float a, DF& sn, DF& cs) {
+  const float k = rintf(__fmul_rn(a, kTwoOverPi));
+  const DF p1 = two_prod(k, kPio2a);
+  DF r = two_sum(__fsub_rn(a, p1.hi), -p1.lo);  // a - p1.hi is exact
+  const DF p2 = two_prod(k, kPio2b);
+  r = df_add(r, DF{-p2.hi, -p2.lo});
+  r = df_add(r, DF{-__fmul_rn(k, kPio2c), 0.f});
+  const DF x = df_mul(r, r);
+  // sin(r) / r = sum_n (-1)^n x^n / (2n+1)!,  cos(r) = sum_n (-1)^n x^n / (2n)!
+  float fs = coef(17, false).hi;
+  fs = __fmaf_rn(fs, x.hi, coef(15, true).hi);
+  fs = __fmaf_rn(fs, x.hi, coef(13, false).hi);
+  fs = __fmaf_rn(fs, x.hi, coef(11, true).hi);
+  DF ps{fs, 0.f};
+  {
+    constexpr Coef c9 = coef(9, false), c7 = coef(7, true), c5 = coef(5, false), c3 = coef(3, true);
+    ps = df_add(df_mul(ps, x), DF{c9.hi, c9.lo});
+    ps = df_add(df_mul(ps, x), DF{c7.hi, c7.lo});
+    ps = df_add(df_mul(ps, x), DF{c5.hi, c5.lo});
+    ps = df_add(df_mul(ps, x), DF{c3.hi, c3.lo});
+    ps = df_add(df_mul(ps, x), DF{1.f, 0.f});
+  }
+  const DF s_r = df_mul(ps, r);
+  float fc = coef(18, true).hi;
+  fc = __fmaf_rn(fc, x.hi, coef(16, false).hi);
+  fc = __fmaf_rn(fc, x.hi, coef(14, true).hi);
+  fc = __fmaf_rn(fc, x.hi, coef(12, false).hi);
+  DF pc{fc, 0.f};
+  {
+    constexpr Coef c10 = coef(10, true), c8 = coef(8, false), c6 = coef(6, true), c4 = coef(4, false),
+                   c2 = coef(2, true);
+    pc = df_add(df_mul(pc, x), DF{c10.hi, c10.lo});
+    pc = df_add(df_mul(pc, x), DF{c8.hi, c8.lo});
+    pc = df_add(df_mul(pc, x), DF{c6.hi, c6.lo});
+    pc = df_add(df_mul(pc, x), DF{c4.hi, c4.lo});
+    pc = df_add(df_mul(pc, x), DF{c2.hi, c2.lo});
+    pc = df_add(df_mul(pc, x), DF{1.f, 0.f});
+  }
+  const DF c_r = pc;
+  const DF ns_r{-s_r.hi, -s_r.lo}, nc_r{-c_r.hi, -c_r.lo};
+  switch (static_cast<int>(k) & 3) {  // a = r + k pi/2
+    case 0: sn = s_r; cs = c_r; break;
+    case 1: sn = c_r; cs = ns_r; break;
+    case 2: sn = ns_r; cs = nc_r; break;
+    default: sn = nc_r; cs = s_r; break;
+  }
+}
+
 // Round hi + lo (|lo| <= half an ulp of hi, hi = RN(hi + lo)) to bf16, nearest even.
 __device__ __forceinline__ uint32_t df_to_bf16(DF v) {
   const uint32_t u = __float_as_uint(v.hi);
@@ -102,23 +200,30 @@ __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendPa
   const int nrot = p.hq + p.hkv;  // rotated heads: queries then keys
   const bool norm_q = p.q_norm_w != nullptr, norm_k = p.k_norm_w != nullptr;
 
-  // ---- per-token coefficients (double precision, once per frequency) ----
+  // ---- per-token coefficients (float pairs, once per frequency) ----
   if (tid < H && pos >= 0) {
     const float a = __fmul_rn(static_cast<float>(pos), p.inv_freq[tid]);
-    double s, c;
-    sincos(static_cast<double>(a), &s, &c);
+    DF sn, cs;
+    if (fabsf(a) < 1048576.f) {
+      sincos_df(a, sn, cs);
+    } else {  // very large angles (positions beyond 2^20): double precision
+      double s, c;
+      sincos(static_cast<double>(a), &s, &c);
+      sn = split(s);
+      cs = split(c);
+    }
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint16_t* w = which == 0 ? p.q_norm_w : p.k_norm_w;
-      double g1 = 1.0, g2 = 1.0;
+      float g1 = 1.f, g2 = 1.f;
       if (w != nullptr) {
-        g1 = static_cast<double>(__uint_as_float(static_cast<uint32_t>(w[tid]) << 16));
-        g2 = static_cast<double>(__uint_as_float(static_cast<uint32_t>(w[tid + H]) << 16));
+        g1 = __uint_as_float(static_cast<uint32_t>(w[tid]) << 16);
+        g2 = __uint_as_float(static_cast<uint32_t>(w[tid + H]) << 16);
       }
-      s_coef[which][0][tid] = split(g1 * c);
-      s_coef[which][1][tid] = split(g2 * s);
-      s_coef[which][2][tid] = split(g2 * c);
-      s_coef[which][3][tid] = split(g1 * s);
+      s_coef[which][0][tid] = df_scale(g1, cs);
+      s_coef[which][1][tid] = df_scale(g2, sn);
+      s_coef[which][2][tid] = df_scale(g2, cs);
+      s_coef[which][3][tid] = df_scale(g1, sn);
     }
   }
   if (tid == kWarps * 32 - 1) {
