@@ -211,6 +211,33 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
                                void* workspace, size_t ws_bytes, int32_t* dev_status,
                                lnk_stream stream);
 
+/*
+ * lnk_paged_decode_attn_static -- lnk_paged_decode_attn without a workspace
+ * argument; it allocates nothing.  (The pages have no counterpart: this is a
+ * calling convention of the library, not a step of the method.)
+ *
+ * For callers that cannot provide scratch memory when the step runs: code run
+ * by a host runtime that has reserved all device memory and forbids allocation
+ * on its execution path, or a serving loop that must keep its memory footprint
+ * and step latency fixed.  The decode scratch lives instead in a static device
+ * array of 8 MiB inside the library, which every GPU that loads the library
+ * keeps until the process exits.  Calls whose lnk_paged_workspace_size(desc, B)
+ * exceeds 8 MiB return LNK_ERANGE and enqueue nothing.
+ *
+ * The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Each call first clears the array's counters on `stream`
+ * (cudaMemsetAsync), then runs the same kernel as lnk_paged_decode_attn.  All
+ * calls share the one array: calls that may run at the same time on the GPU
+ * (different streams or host threads) race and must be ordered by the caller.
+ * Arguments, layouts and errors are otherwise those of lnk_paged_decode_attn.
+ */
+lnk_status lnk_paged_decode_attn_static(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
+                                        const int32_t* positions, const int32_t* table,
+                                        const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                                        lnk_bf16* out, int32_t B, int32_t* dev_status,
+                                        lnk_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

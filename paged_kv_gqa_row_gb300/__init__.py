@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     attn_desc,
     lnk_paged_append_rope,
     lnk_paged_decode_attn,
+    lnk_paged_decode_attn_static,
     lnk_paged_step_attn,
     lnk_paged_workspace_size,
     lnk_rope_inv_freq,

@@ -28,7 +28,8 @@ DEV_BAD_ROW, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_BAD_SLOT = 0x01, 0x02, 0x04, 0x
 DEV_SEGMENT, DEV_BAD_LAST, DEV_TIMEOUT = 0x10, 0x20, 0x40
 
 EXPORTED = ["lnk_status_string", "lnk_rope_inv_freq", "lnk_paged_workspace_size",
-            "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_step_attn"]
+            "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_step_attn",
+            "lnk_paged_decode_attn_static"]
 
 
 class LnkError(RuntimeError):
@@ -63,6 +64,9 @@ _lib.lnk_paged_append_rope.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(
 _lib.lnk_paged_decode_attn.restype = ctypes.c_int
 _lib.lnk_paged_decode_attn.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                        c_i32, c_vp, c_size, c_vp, c_vp]
+_lib.lnk_paged_decode_attn_static.restype = ctypes.c_int
+_lib.lnk_paged_decode_attn_static.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                              c_i32, c_vp, c_vp]
 _lib.lnk_paged_step_attn.restype = ctypes.c_int
 _lib.lnk_paged_step_attn.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                      c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_size,
@@ -133,6 +137,15 @@ def lnk_paged_decode_attn(desc, q_roped, positions, table, k_pool, v_pool, out, 
                                     _ptr(k_pool), _ptr(v_pool), _ptr(out), B, _ptr(workspace),
                                     ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "lnk_paged_decode_attn")
+
+
+def lnk_paged_decode_attn_static(desc, q_roped, positions, table, k_pool, v_pool, out, B,
+                                 dev_status=None, stream=None):
+    """lnk_paged_decode_attn with the library's own static scratch (no workspace)."""
+    st = _lib.lnk_paged_decode_attn_static(ctypes.byref(desc), _ptr(q_roped), _ptr(positions), _ptr(table),
+                                           _ptr(k_pool), _ptr(v_pool), _ptr(out), B, _ptr(dev_status),
+                                           _stream(stream))
+    _check(st, "lnk_paged_decode_attn_static")
 
 
 def lnk_paged_step_attn(desc, q_roped, rows, positions, segments, step_positions, table, k_pool,
