@@ -222,7 +222,7 @@ def run_reference(args, rank, world):
     import synth
     if rank != 0:
         return None
-    w = synth.build(args.config)
+    w = synth.build(args.config, scale=args.scale, rows=args.rows)
     rng = np.random.default_rng(0)
     rows = sorted(rng.choice(w.B, size=min(w.B, args.ref_rows), replace=False).tolist())
     for _ in range(max(0, args.warmup)):
@@ -260,7 +260,7 @@ def run_gpu(args, rank, world, dist):
     dev = torch.device("cuda", local)
     seed = None if rank == 0 else 1000 + 97 * rank + {"phi3_tiny": 1, "mistral": 2, "phi3_window": 3,
                                                        "qwen3": 4, "llama_step": 5}[args.config]
-    w = synth.build(args.config, seed=seed)
+    w = synth.build(args.config, seed=seed, scale=args.scale, rows=args.rows)
     parts = algorithmic_bytes(w)
     pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * 2
     copies = args.pool_copies or (2 if pool_bytes < (8 << 30) else 1)
@@ -417,7 +417,7 @@ def run_gpu(args, rank, world, dist):
         "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIGS[args.config],
-                   "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
+                   "scale": args.scale, "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.head_dim, "page_size": 64, "num_pages": w.num_pages,
                    "parallelism": f"rows x{world} (independent batches per GPU)",
                    "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e9:.2f} GB, "
@@ -462,6 +462,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-copies", type=int, default=0, help="pool copies alternated step to step (0: auto)")
+    ap.add_argument("--scale", type=float, default=1.0, help="shrink context lengths (profiling runs only)")
+    ap.add_argument("--rows", type=int, default=None, help="override the number of decode rows (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
