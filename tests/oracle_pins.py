@@ -442,3 +442,27 @@ def pin_cache_size():
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+def pin_decode_rows_is_identity_table():
+    """Row-based decode over contiguous caches (each row its own MaxSeq positions)
+    is paged decode with an identity table: row b's page j is page b * pages + j."""
+    rng = np.random.default_rng(13)
+    rows, pages, d = 3, 4, 16
+    cache_k = _rand_bits(rng, (rows, 2, pages * 64, d))   # [Batch, Heads, MaxSeq, D]
+    cache_v = _rand_bits(rng, (rows, 2, pages * 64, d))
+    pos = np.array([200, 0, 255])
+    q = _rand_bits(rng, (rows, 4, d))
+    # the pool is the caches' rows laid end to end per head
+    kp = np.concatenate([cache_k[b] for b in range(rows)], axis=1)
+    vp = np.concatenate([cache_v[b] for b in range(rows)], axis=1)
+    table = (np.arange(rows)[:, None] * pages + np.arange(pages)[None, :]).astype(np.int32)
+    paged_out = paged.decode_attention(q, pos, table, kp, vp, 0)
+    for b in range(rows):
+        # decode_rows: row b attends over cache row b, positions 0..pos[b]
+        ident = np.arange(pages, dtype=np.int32)[None, :]
+        row_out = paged.attention_at(q[b], 0, int(pos[b]), ident, cache_k[b], cache_v[b], 0)
+        assert np.array_equal(row_out, paged_out[b])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

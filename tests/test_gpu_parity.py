@@ -351,3 +351,42 @@ def test_repeatable():
     dev.step()
     _sync()
     assert np.array_equal(a, to_bits(dev.out))
+
+
+def test_decode_rows_over_contiguous_caches():
+    """decode_rows (contiguous cache rows of MaxSeq positions) through the paged
+    call with an identity table, against the oracle's row-by-row attention."""
+    import paged_kv_gqa_row_gb300 as lnk
+    from oracle import bf16, paged, rope
+    rng = np.random.default_rng(21)
+    rows, max_seq, hq, hkv, d = 5, 1024, 8, 2, 128
+    pages = max_seq // 64
+    ck = bf16.from_f64(rng.standard_normal((rows, hkv, max_seq, d)))
+    cv = bf16.from_f64(rng.standard_normal((rows, hkv, max_seq, d)))
+    pos = np.array([1023, 0, 64, 500, 63], dtype=np.int32)
+    q = bf16.from_f64(rng.standard_normal((rows, hq, d)))
+    k = bf16.from_f64(rng.standard_normal((rows, hkv, d)))
+    v = bf16.from_f64(rng.standard_normal((rows, hkv, d)))
+    pool_k = np.concatenate([ck[b] for b in range(rows)], axis=1)
+    pool_v = np.concatenate([cv[b] for b in range(rows)], axis=1)
+    table = (np.arange(rows)[:, None] * pages + np.arange(pages)[None, :]).astype(np.int32)
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    dk, dv = t16(pool_k), t16(pool_v)
+    dq, dkk, dvv, dpos, dtab = t16(q), t16(k), t16(v), t32(pos), t32(table)
+    q_out = torch.zeros_like(dq)
+    out = torch.zeros_like(dq)
+    desc = lnk.attn_desc(hq, hkv, d, rows * pages, rows, pages)
+    rd = lnk.rope_desc(500000.0)
+    ws_bytes = lnk.lnk_paged_workspace_size(desc, rows)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    lnk.lnk_paged_append_rope(desc, rd, dq, dkk, dvv, dpos, None, None, dtab, None, None, 1e-6, dk, dv, q_out, rows)
+    lnk.lnk_paged_decode_attn(desc, q_out, dpos, dtab, dk, dv, out, rows, ws, ws_bytes)
+    torch.cuda.synchronize()
+    inv = rope.inv_freq(500000.0, d)
+    ident = np.arange(pages, dtype=np.int32)[None, :]
+    got = to_bits(out)
+    for b in range(rows):
+        qo, ck_b, cv_b = paged.append_rope(q[[b]], k[[b]], v[[b]], pos[[b]], [0], ident, ck[b], cv[b], inv)
+        want = paged.attention_at(qo[0], 0, int(pos[b]), ident, ck_b, cv_b, 0)
+        assert_attention_close(got[b], want, f"row {b}")
