@@ -1,17 +1,31 @@
-// K4: packed prompt chunks (prefill_paged / the prompt part of step_paged).
+// K4: packed prompt chunks (prefill_paged / the prompt part of step_paged) on
+// the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Every chunk token attends over its own row's pages up to its position (and
 // the window).  A CTA takes one tile of consecutive pack tokens and one kv
 // head: tile_tokens = 128 / G tokens times the G query heads of that kv head
-// gives 128 query rows, 16 per consumer warp (row m = token * G + head).
-// Tokens of a tile are grouped into runs of equal table rows; for each run
-// the producer warp streams the row's pages covering the run's key range
-// through a ring of TMA stages (128-byte swizzle), and the eight consumer
-// warps run the FlashAttention recurrence per page:
-//   S[16 rows, 64 keys]  = Q K^T   (mma m16n8k16, K^T fragments via ldmatrix)
-//   O[16 rows, D]       += P V     (P reused from the S accumulators,
-//                                   V fragments via ldmatrix.trans)
-// with a per-row mask: same run, lo <= key <= position.
+// gives 128 query rows (row m = token * G + head), one tensor-memory lane each.
+// Tokens of a tile are grouped into runs of equal table rows; for each run the
+// pages covering the run's key range are streamed through the kernel.
+//
+// CTA structure (192 threads, warp-specialised):
+//  * warp 0, producer: loads the tile's queries once (3-D TMA box of
+//    tokens x G heads x 64 columns) and each page's K and V (2-D TMA boxes,
+//    128-byte swizzle) into a ring of stages;
+//  * warp 1, MMA: one thread issues, per page j,
+//      S_j[128 x 64]  = Q K_j^T          (tcgen05.mma, both operands in shared
+//                                         memory, K-major; S double-buffered in
+//                                         tensor memory)
+//      O[128 x D]    += P_j V_j          (P_j from tensor memory as bf16, V_j
+//                                         MN-major in shared memory)
+//    S_{j+1} is issued before P_j V_j so that the tensor core works while the
+//    softmax handles page j; commits release stages and signal the softmax;
+//  * warps 2-5, softmax: thread r owns query row r (tensor-memory lane r):
+//    reads its 64 scores, masks them (same run, lo <= key <= position),
+//    updates the running max and sum in registers, writes P_j back to tensor
+//    memory, and rescales its row of O only when the running max grows by more
+//    than 2^8 (until then P stays below 256, exact enough in bf16); at the end
+//    it normalises its row of O and stores it.
 //
 // Sources: "Mistral 7B Instruct v0.3", Entries table (prefill_paged: prompts
 // packed end to end, each token written at its place in the pool and attending
@@ -24,42 +38,54 @@
 namespace lnk {
 namespace {
 
-constexpr int kWarps = 8;                  // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kStages = 4;
-constexpr int kRows = kWarps * 16;         // query rows per tile
+constexpr int kThreads = 6 * 32;
+constexpr int kStages = 3;
+constexpr int kRows = 128;               // query rows per tile = tensor-memory lanes
+constexpr float kRescaleLog2 = 8.f;      // rescale O when the max grows by more than 2^8
 
-struct ChunkStage {
-  int run, key_base, valid;
+struct PageInfo {
+  int run, key_base, valid, pad;
 };
 
 template <int D>
-struct ChunkSmem {
+struct TcSmem {
   static constexpr int NB = boxes_for(D);
-  static constexpr int kStageBytes = 2 * NB * kBoxBytes;
-  static constexpr size_t stages = 0;
+  static constexpr int kQBytes = NB * kRows * 128;          // query tile: NB boxes of 128 rows x 128 B
+  static constexpr int kStageBytes = 2 * NB * kBoxBytes;    // K boxes, then V boxes
+  static constexpr int kPvN = D <= 64 ? 64 : 128;           // N of the P.V product (D = 96 padded)
+  static constexpr uint32_t kTmemCols = D <= 64 ? 256 : 512;
+  // tensor-memory columns
+  static constexpr uint32_t kColS0 = 0, kColS1 = 64, kColP0 = 128, kColP1 = 160, kColO = 192;
+  static constexpr size_t q = 0;
+  static constexpr size_t stages = q + kQBytes;
   static constexpr size_t bars = stages + size_t(kStages) * kStageBytes;
-  static constexpr size_t info = bars + (2 * kStages + 1) * sizeof(uint64_t);
-  static constexpr size_t tok = info + kStages * sizeof(ChunkStage);
-  static constexpr size_t runs = tok + 3 * kRows * 4;     // token lo, hi (exclusive), run
-  static constexpr size_t misc = runs + 4 * kRows * 4;    // run row, kmin, kmax, pages
-  static constexpr size_t bytes = misc + 64 + 1024;
+  // full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], zero
+  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr size_t info = bars + kNumBars * sizeof(uint64_t);
+  static constexpr size_t tok = info + kStages * sizeof(PageInfo);
+  static constexpr size_t runs = tok + 3 * kRows * 4;
+  static constexpr size_t misc = runs + 4 * kRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base
+  // at least 100 KiB so that no more CTAs share an SM than its tensor memory holds
+  static constexpr size_t bytes = (misc + 64 + 1024) > 102400 ? (misc + 64 + 1024) : 102400;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                 const ChunkParams p) {
-  using L = ChunkSmem<D>;
+    chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap, const ChunkParams p) {
+  using L = TcSmem<D>;
   constexpr int NB = L::NB;
-  constexpr int DK = D / 16;   // k-steps of Q K^T
-  constexpr int DN = D / 8;    // n-tiles of the output
+  constexpr int DK = D / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* zero_bar = empty_bar + kStages;  // consumers finished zeroing a partial page
-  ChunkStage* info = reinterpret_cast<ChunkStage*>(smem + L::info);
+  uint64_t* q_full = empty_bar + kStages;
+  uint64_t* s_full = q_full + 1;    // [2]
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* pv_done = p_full + 2;   // [2]
+  uint64_t* zero_bar = pv_done + 2;
+  PageInfo* info = reinterpret_cast<PageInfo*>(smem + L::info);
   int* tok_lo = reinterpret_cast<int*>(smem + L::tok);
   int* tok_hi = tok_lo + kRows;
   int* tok_run = tok_hi + kRows;
@@ -67,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* run_kmin = run_row + kRows;
   int* run_kmax = run_kmin + kRows;
   int* run_pages = run_kmax + kRows;
-  int* misc = reinterpret_cast<int*>(smem + L::misc);  // [0] runs, [1] stages, [2] abort
+  int* misc = reinterpret_cast<int*>(smem + L::misc);
   volatile int* abort_flag = misc + 2;
 
   const int tid = threadIdx.x;
@@ -83,12 +109,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(full_bar + s), 1);
-      mbar_init(smem_addr(empty_bar + s), kWarps);
+      mbar_init(smem_addr(empty_bar + s), 1);
     }
-    mbar_init(smem_addr(zero_bar), kWarps * 32);
+    mbar_init(smem_addr(q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(s_full + i), 1);
+      mbar_init(smem_addr(p_full + i), 4);
+      mbar_init(smem_addr(pv_done + i), 1);
+    }
+    mbar_init(smem_addr(zero_bar), kRows);
     misc[2] = 0;
     fence_mbarrier_init();
   }
+  if (warp == 1) tmem_alloc(smem_addr(misc + 3), L::kTmemCols);
   // ---- tokens of the tile ----
   if (tid < TQ) {
     int lo = 0, hi = 0, bad = 0;
@@ -114,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (tid == 0) {
-    int nr = 0, cur = -1, stages = 0;
+    int nr = 0, cur = -1, pages = 0;
     for (int i = 0; i < nt; ++i) {
       if (tok_hi[i] <= tok_lo[i]) {
         tok_run[i] = -1;
@@ -135,241 +168,279 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = nt; i < TQ; ++i) tok_run[i] = -1;
     for (int r = 0; r < nr; ++r) {
       run_pages[r] = (run_kmax[r] - 1) / kPage - run_kmin[r] / kPage + 1;
-      stages += run_pages[r];
+      pages += run_pages[r];
     }
     misc[0] = nr;
-    misc[1] = stages;
+    misc[1] = pages;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   const int nruns = misc[0];
-  const int nstages = misc[1];
+  const int npages = misc[1];
+  const uint32_t tmem = static_cast<uint32_t>(misc[3]);
 
-  if (warp == kWarps) {
+  if (warp == 0) {
     // ============================== producer ==============================
-    if (lane != 0) return;
-    tma_prefetch_descriptor(&kmap);
-    tma_prefetch_descriptor(&vmap);
-    int k = 0;
-    bool stop = false;
-    for (int run = 0; run < nruns && !stop; ++run) {
-      const int* trow = p.table + static_cast<long long>(run_row[run]) * p.pages_per_row;
-      const int first = run_kmin[run] / kPage;
-      for (int j = 0; j < run_pages[run]; ++j, ++k) {
-        const int s = k % kStages;
-        if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
-          stop = true;
-          break;
-        }
-        const int lp = first + j;
-        const int page = trow[lp];
-        const uint32_t fb = smem_addr(full_bar + s);
-        ChunkStage si{run, lp * kPage, 1};
-        if (page < 0 || page >= p.num_pages) {
-          if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
-          si.valid = 0;
-          info[s] = si;
-          mbar_arrive(fb);
-        } else {
-          info[s] = si;
-          mbar_arrive_expect_tx(fb, L::kStageBytes);
-          const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
-          const uint32_t vdst = kdst + NB * kBoxBytes;
-          const int y = (h * p.num_pages + page) * kPage;
+    if (lane == 0 && npages > 0) {
+      tma_prefetch_descriptor(&qmap);
+      const uint32_t qb = smem_addr(q_full);
+      mbar_arrive_expect_tx(qb, L::kQBytes);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
-            tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
+      for (int nb = 0; nb < NB; ++nb)
+        tma_load_3d(smem_addr(smem + L::q + nb * kRows * 128), &qmap, nb * kBoxCols, h * G, t0, qb);
+      int k = 0;
+      bool stop = false;
+      for (int run = 0; run < nruns && !stop; ++run) {
+        const int* trow = p.table + static_cast<long long>(run_row[run]) * p.pages_per_row;
+        const int first = run_kmin[run] / kPage;
+        for (int j = 0; j < run_pages[run]; ++j, ++k) {
+          const int s = k % kStages;
+          if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          const int lp = first + j;
+          const int page = trow[lp];
+          const uint32_t fb = smem_addr(full_bar + s);
+          PageInfo si{run, lp * kPage, 1, 0};
+          if (page < 0 || page >= p.num_pages) {
+            if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
+            si.valid = 0;
+            info[s] = si;
+            mbar_arrive(fb);
+          } else {
+            info[s] = si;
+            mbar_arrive_expect_tx(fb, L::kStageBytes);
+            const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+            const uint32_t vdst = kdst + NB * kBoxBytes;
+            const int y = (h * p.num_pages + page) * kPage;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
+              tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
+            }
           }
         }
       }
-    }
-    const int issued = k;
-    for (int kk = max(0, issued - kStages); kk < issued; ++kk) {
-      const uint32_t fb = smem_addr(full_bar + kk % kStages);
-      const uint64_t t_0 = global_timer_ns();
-      while (!mbar_try_wait(fb, (kk / kStages) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+      // do not leave while a copy may still land in this CTA's memory
+      const int issued = k;
+      for (int kk = max(0, issued - kStages); kk < issued; ++kk) {
+        const uint32_t fb = smem_addr(full_bar + kk % kStages);
+        const uint64_t t_0 = global_timer_ns();
+        while (!mbar_try_wait(fb, (kk / kStages) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+        }
       }
     }
-    if (*abort_flag && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
-    return;
-  }
-
-  // ============================== consumers ==============================
-  const int c = lane & 3;
-  const int r = lane >> 2;
-  const int m0 = warp * 16 + r, m1 = m0 + 8;
-  const int tk0 = m0 / G, g0 = m0 % G;
-  const int tk1 = m1 / G, g1 = m1 % G;
-  const int lo0 = tok_lo[tk0], hi0 = tok_hi[tk0], run0 = tok_run[tk0];
-  const int lo1 = tok_lo[tk1], hi1 = tok_hi[tk1], run1 = tok_run[tk1];
-
-  // Q fragments (A operand, rows m0 / m1)
-  uint32_t qa[DK][4];
-  {
-    const uint16_t* q0 = p.q + (static_cast<size_t>(t0 + tk0) * p.hq + static_cast<size_t>(h) * G + g0) * D;
-    const uint16_t* q1 = p.q + (static_cast<size_t>(t0 + tk1) * p.hq + static_cast<size_t>(h) * G + g1) * D;
-    const bool ok0 = run0 >= 0, ok1 = run1 >= 0;
+  } else if (warp == 1) {
+    // ================================ MMA =================================
+    if (lane == 0 && npages > 0) {
+      constexpr uint32_t kIdS = umma_idesc_bf16(kRows, 64, 0, 0);
+      constexpr uint32_t kIdPV = umma_idesc_bf16(kRows, L::kPvN, 0, 1);
+      const uint32_t qaddr = smem_addr(smem + L::q);
+      bool ok = mbar_wait(smem_addr(q_full), 0, abort_flag);
+      tc_fence_after();
+      int last_pv = -1;
+      for (int j = 0; ok && j <= npages; ++j) {
+        if (j < npages) {
+          const int s = j % kStages, b = j & 1;
+          if (!mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
 #pragma unroll
-    for (int kk = 0; kk < DK; ++kk) {
-      const int e = kk * 16 + 2 * c;
-      qa[kk][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + e) : 0u;
-      qa[kk][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + e) : 0u;
-      qa[kk][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + e + 8) : 0u;
-      qa[kk][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + e + 8) : 0u;
+          for (int kk = 0; kk < DK; ++kk) {
+            const uint64_t ad = umma_desc_sw128(qaddr + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 0, 1024);
+            const uint64_t bd = umma_desc_sw128(kaddr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 0, 1024);
+            umma_ss(tmem + (b ? L::kColS1 : L::kColS0), ad, bd, kIdS, kk > 0);
+          }
+          umma_commit(smem_addr(s_full + b));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % kStages, b = jj & 1;
+          if (!mbar_wait(smem_addr(p_full + b), (jj >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t vaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes) + NB * kBoxBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // 64 keys, 16 per instruction
+            const uint64_t bd = umma_desc_sw128(vaddr + kk * 16 * 128, kBoxBytes, 1024);
+            umma_ts(tmem + L::kColO, tmem + (b ? L::kColP1 : L::kColP0) + kk * 8, bd, kIdPV, (jj > 0 || kk > 0));
+          }
+          umma_commit(smem_addr(empty_bar + s));
+          umma_commit(smem_addr(pv_done + b));
+          last_pv = jj;
+        }
+      }
+      // the tensor memory is freed at the end: let the last product finish
+      if (last_pv >= 0) {
+        const uint32_t bar = smem_addr(pv_done + (last_pv & 1));
+        const uint64_t t_0 = global_timer_ns();
+        while (!mbar_try_wait(bar, (last_pv >> 1) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+        }
+      }
     }
-  }
-  float o[DN][4];
-#pragma unroll
-  for (int n = 0; n < DN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_0 = -INFINITY, m_1 = -INFINITY, l_0 = 0.f, l_1 = 0.f;
-  uint32_t zero_phase = 0;
-
-  for (int k = 0; k < nstages; ++k) {
-    const int s = k % kStages;
-    if (!mbar_wait(smem_addr(full_bar + s), (k / kStages) & 1, abort_flag)) break;
-    const ChunkStage si = info[s];
-    const uint8_t* kbuf = smem + L::stages + size_t(s) * L::kStageBytes;
-    const uint8_t* vbuf = kbuf + NB * kBoxBytes;
-    const int kb = si.key_base;
-    if (si.valid) {
+  } else {
+    // ============================== softmax ===============================
+    const int qt = warp & 3;              // tensor-memory lane quarter of this warp
+    const int row = qt * 32 + lane;       // query row = token * G + head
+    const int tl = row / G, g = row % G;
+    const int lo = tok_lo[tl], hi = tok_hi[tl], run_id = tok_run[tl];
+    const bool live = tl < nt && run_id >= 0;
+    const uint32_t lane_addr = static_cast<uint32_t>(qt * 32) << 16;
+    const int ctid = tid - 64;            // 0..127 among the softmax threads
+    float m_ref = -INFINITY, l_sum = 0.f;
+    uint32_t zero_uses = 0;
+    bool ok = true;
+    for (int j = 0; j < npages && ok; ++j) {
+      const int s = j % kStages, b = j & 1;
+      ok = mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag);
+      if (!ok) break;
+      const PageInfo si = info[s];
       const int kmin = run_kmin[si.run], kmax = run_kmax[si.run];
-      if (kb < kmin || kb + kPage > kmax) {
+      if (!si.valid || si.key_base < kmin || si.key_base + kPage > kmax) {
         // Keys of this page outside the run's range may hold stale or
-        // uninitialised data: zero their value rows before anyone reads them.
-        uint8_t* vw = const_cast<uint8_t*>(vbuf);
-        for (int i = tid; i < kPage * NB * 8; i += kWarps * 32) {
-          const int key = i / (NB * 8);
-          const int rest = i % (NB * 8);
-          if (kb + key < kmin || kb + key >= kmax)
-            *reinterpret_cast<uint4*>(vw + (rest >> 3) * kBoxBytes + key * 128 + (rest & 7) * 16) =
+        // uninitialised data: zero their value rows before P.V reads them.
+        uint8_t* vb = smem + L::stages + size_t(s) * L::kStageBytes + NB * kBoxBytes;
+        for (int i = ctid; i < kPage * NB * 8; i += kRows) {
+          const int key = i / (NB * 8), rest = i % (NB * 8);
+          if (!si.valid || si.key_base + key < kmin || si.key_base + key >= kmax)
+            *reinterpret_cast<uint4*>(vb + (rest >> 3) * kBoxBytes + key * 128 + (rest & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(zero_bar));
-        if (!mbar_wait(smem_addr(zero_bar), zero_phase & 1, abort_flag)) break;
-        ++zero_phase;
+        ok = mbar_wait(smem_addr(zero_bar), zero_uses & 1u, abort_flag);
+        ++zero_uses;
       }
-    }
-    // does any row of this warp see a key of this page?
-    const bool in0 = run0 == si.run && lo0 < kb + kPage && hi0 > kb;
-    const bool in1 = run1 == si.run && lo1 < kb + kPage && hi1 > kb;
-    if (si.valid && __any_sync(0xffffffffu, in0 || in1)) {
-      const uint32_t kaddr = smem_addr(kbuf);
-      const uint32_t vaddr = smem_addr(vbuf);
-      float sc[8][4];
+      if (!ok) break;
+      ok = mbar_wait(smem_addr(s_full + b), (j >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      float x[64];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_addr + (b ? L::kColS1 : L::kColS0) + c * 16, r);
+        tmem_ld_wait();
 #pragma unroll
-      for (int kk = 0; kk < DK; ++kk) {
+        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(r[i]);
+      }
+      const bool in_run = live && si.valid && si.run == run_id;
+      float mx = -INFINITY;
 #pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
-          const int key = nn * 16 + (lane & 7) + (lane >> 4) * 8;
-          const int chunk = kk * 2 + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kaddr + (chunk >> 3) * kBoxBytes + swz128(key, chunk & 7), b0, b1, b2, b3);
-          mma_bf16_16816(sc[2 * nn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma_bf16_16816(sc[2 * nn + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+      for (int i = 0; i < 64; ++i) {
+        const int key = si.key_base + i;
+        const bool v = in_run && key >= lo && key < hi;
+        x[i] = v ? x[i] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[i]);
+      }
+      // running max: rescale O only when it grows by more than 2^8
+      float alpha = 1.f;
+      if (mx != -INFINITY) {
+        if (m_ref == -INFINITY) {
+          m_ref = mx;
+        } else if (mx > m_ref + kRescaleLog2) {
+          alpha = exp2f(m_ref - mx);
+          m_ref = mx;
+          l_sum *= alpha;
         }
       }
-      // mask + row maxima
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (__any_sync(0xffffffffu, alpha != 1.f) && j >= 1) {
+        const int jp = j - 1;
+        ok = mbar_wait(smem_addr(pv_done + (jp & 1)), (jp >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < L::kPvN / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_addr + L::kColO + c * 16, r);
+          tmem_ld_wait();
+          uint32_t w0[8], w1[8];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int key = kb + n * 8 + 2 * c;
-        const bool a0 = in0 && key >= lo0 && key < hi0;
-        const bool a1 = in0 && key + 1 >= lo0 && key + 1 < hi0;
-        const bool b0 = in1 && key >= lo1 && key < hi1;
-        const bool b1 = in1 && key + 1 >= lo1 && key + 1 < hi1;
-        sc[n][0] = a0 ? sc[n][0] * p.scale_log2 : -INFINITY;
-        sc[n][1] = a1 ? sc[n][1] * p.scale_log2 : -INFINITY;
-        sc[n][2] = b0 ? sc[n][2] * p.scale_log2 : -INFINITY;
-        sc[n][3] = b1 ? sc[n][3] * p.scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+          for (int i = 0; i < 8; ++i) {
+            w0[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            w1[i] = __float_as_uint(__uint_as_float(r[8 + i]) * alpha);
+          }
+          tmem_st8(tmem + lane_addr + L::kColO + c * 16, w0);
+          tmem_st8(tmem + lane_addr + L::kColO + c * 16 + 8, w1);
+        }
+        tmem_st_wait();
       }
+      // probabilities relative to m_ref, packed to bf16
+      const float base = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[32];
+      float rs = 0.f;
 #pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      for (int i = 0; i < 32; ++i) {
+        const float e0 = exp2f(x[2 * i] - base), e1 = exp2f(x[2 * i + 1] - base);
+        rs += e0 + e1;
+        pk[i] = pack_bf16x2(e0, e1);
       }
-      const float mn0 = fmaxf(m_0, mx0), mn1 = fmaxf(m_1, mx1);
-      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m_0 - base0), al1 = exp2f(m_1 - base1);
-      m_0 = mn0;
-      m_1 = mn1;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const float e0 = exp2f(sc[n][0] - base0), e1 = exp2f(sc[n][1] - base0);
-        const float e2 = exp2f(sc[n][2] - base1), e3 = exp2f(sc[n][3] - base1);
-        rs0 += e0 + e1;
-        rs1 += e2 + e3;
-        // A fragment of P for k-step n / 2: n even -> regs 0, 1; n odd -> regs 2, 3
-        pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16x2(e0, e1);
-        pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16x2(e2, e3);
+      l_sum += rs;
+      if (j >= 2) {  // P buffer b was last read by P.V of page j - 2
+        ok = mbar_wait(smem_addr(pv_done + b), ((j - 2) >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
       }
-      l_0 = l_0 * al0 + rs0;
-      l_1 = l_1 * al1 + rs1;
+      const uint32_t pcol = b ? L::kColP1 : L::kColP0;
 #pragma unroll
-      for (int n = 0; n < DN; ++n) {
-        o[n][0] *= al0;
-        o[n][1] *= al0;
-        o[n][2] *= al1;
-        o[n][3] *= al1;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pk[c * 8 + i];
+        tmem_st8(tmem + lane_addr + pcol + c * 8, w);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(p_full + b));
+    }
+    // ---- normalise and store this row ----
+    if (ok && npages > 0) {
+      const int jl = npages - 1;
+      ok = mbar_wait(smem_addr(pv_done + (jl & 1)), (jl >> 1) & 1, abort_flag);
+      tc_fence_after();
+    }
+    uint16_t* dst = p.out + (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
+    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < L::kPvN / 16; ++c) {
+      uint32_t r[16];
+      if (ok && npages > 0) {
+        tmem_ld16(tmem + lane_addr + L::kColO + c * 16, r);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      }
+      if (tl < nt && c * 16 < D) {
+        uint2* o = reinterpret_cast<uint2*>(dst + c * 16);
 #pragma unroll
-        for (int nd = 0; nd < DN / 2; ++nd) {
-          const int key = j * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int chunk = nd * 2 + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vaddr + (chunk >> 3) * kBoxBytes + swz128(key, chunk & 7), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * nd], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b0, b1);
-          mma_bf16_16816(o[2 * nd + 1], pa[j][0], pa[j][1], pa[j][2], pa[j][3], b2, b3);
+        for (int i = 0; i < 4; ++i) {
+          const float a0 = live ? __uint_as_float(r[4 * i]) * inv : 0.f;
+          const float a1 = live ? __uint_as_float(r[4 * i + 1]) * inv : 0.f;
+          const float a2 = live ? __uint_as_float(r[4 * i + 2]) * inv : 0.f;
+          const float a3 = live ? __uint_as_float(r[4 * i + 3]) * inv : 0.f;
+          o[i] = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(empty_bar + s));
   }
-  if (*abort_flag) {
-    if (lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
-  }
-
-  // ---- normalise and store ----
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    l_0 += __shfl_xor_sync(0xffffffffu, l_0, off);
-    l_1 += __shfl_xor_sync(0xffffffffu, l_1, off);
-  }
-  const float inv0 = l_0 > 0.f ? 1.f / l_0 : 0.f;
-  const float inv1 = l_1 > 0.f ? 1.f / l_1 : 0.f;
-  if (tk0 < nt) {
-    uint16_t* dst = p.out + (static_cast<size_t>(t0 + tk0) * p.hq + static_cast<size_t>(h) * G + g0) * D;
-#pragma unroll
-    for (int n = 0; n < DN; ++n)
-      *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * c) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
-  }
-  if (tk1 < nt) {
-    uint16_t* dst = p.out + (static_cast<size_t>(t0 + tk1) * p.hq + static_cast<size_t>(h) * G + g1) * D;
-#pragma unroll
-    for (int n = 0; n < DN; ++n)
-      *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * c) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
-  }
+  if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 template <int D>
-cudaError_t launch_chunk_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
-                           cudaStream_t stream) {
-  const int bytes = static_cast<int>(ChunkSmem<D>::bytes);
+cudaError_t launch_chunk_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const ChunkParams& p, cudaStream_t stream) {
+  const int bytes = static_cast<int>(TcSmem<D>::bytes);
   cudaError_t err =
       cudaFuncSetAttribute(chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_tiles, p.hkv);
-  chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(kmap, vmap, p);
+  chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 
@@ -385,13 +456,13 @@ __global__ void gather_last_kernel(const uint16_t* out, const int32_t* last, uin
 
 }  // namespace
 
-cudaError_t launch_chunk(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
-                         int head_dim, cudaStream_t stream) {
+cudaError_t launch_chunk(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const ChunkParams& p, int head_dim, cudaStream_t stream) {
   if (p.P == 0) return cudaSuccess;
   switch (head_dim) {
-    case 64: return launch_chunk_t<64>(kmap, vmap, p, stream);
-    case 96: return launch_chunk_t<96>(kmap, vmap, p, stream);
-    case 128: return launch_chunk_t<128>(kmap, vmap, p, stream);
+    case 64: return launch_chunk_t<64>(qmap, kmap, vmap, p, stream);
+    case 96: return launch_chunk_t<96>(qmap, kmap, vmap, p, stream);
+    case 128: return launch_chunk_t<128>(qmap, kmap, vmap, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

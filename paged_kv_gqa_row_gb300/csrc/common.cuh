@@ -83,8 +83,8 @@ struct ChunkParams {
   float scale_log2;
 };
 
-cudaError_t launch_chunk(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
-                         int head_dim, cudaStream_t stream);
+cudaError_t launch_chunk(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const ChunkParams& p, int head_dim, cudaStream_t stream);
 
 // ------------------------------------------------------------ gather last --
 cudaError_t launch_gather_last(const uint16_t* out, const int32_t* last, uint16_t* last_out, int M,
