@@ -316,23 +316,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       float x[64];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_addr + (b ? L::kColS1 : L::kColS0) + c * 16, r);
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_addr + (b ? L::kColS1 : L::kColS0), r0);
+        tmem_ld32(tmem + lane_addr + (b ? L::kColS1 : L::kColS0) + 32, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(r0[i]);
+          x[32 + i] = __uint_as_float(r1[i]);
+        }
       }
+      // visible keys of this page for this row: [ka, ke)
       const bool in_run = live && si.valid && si.run == run_id;
-      float mx = -INFINITY;
+      const int ka = in_run ? max(lo - si.key_base, 0) : kPage;
+      const int ke = in_run ? max(ka, min(hi - si.key_base, kPage)) : kPage;
+      float mraw = -INFINITY;
+      if (__all_sync(0xffffffffu, ka == 0 && ke == kPage)) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int key = si.key_base + i;
-        const bool v = in_run && key >= lo && key < hi;
-        x[i] = v ? x[i] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, x[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = (i >= ka && i < ke) ? x[i] : -INFINITY;
+          mraw = fmaxf(mraw, x[i]);
+        }
       }
+      const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;  // log2 units
       // running max: rescale O only when it grows by more than 2^8
       float alpha = 1.f;
       if (mx != -INFINITY) {
@@ -350,28 +360,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < L::kPvN / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_addr + L::kColO + c * 16, r);
+        for (int c = 0; c < L::kPvN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + L::kColO + c * 32, r);
           tmem_ld_wait();
-          uint32_t w0[8], w1[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            w0[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            w1[i] = __float_as_uint(__uint_as_float(r[8 + i]) * alpha);
-          }
-          tmem_st8(tmem + lane_addr + L::kColO + c * 16, w0);
-          tmem_st8(tmem + lane_addr + L::kColO + c * 16 + 8, w1);
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tmem + lane_addr + L::kColO + c * 32, r);
         }
         tmem_st_wait();
       }
-      // probabilities relative to m_ref, packed to bf16
-      const float base = m_ref == -INFINITY ? 0.f : m_ref;
+      // probabilities 2^(s * scale * log2(e) - m_ref), packed to bf16
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       uint32_t pk[32];
       float rs = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float e0 = exp2f(x[2 * i] - base), e1 = exp2f(x[2 * i + 1] - base);
+        const float e0 = ex2_approx(__fmaf_rn(x[2 * i], p.scale_log2, nbase));
+        const float e1 = ex2_approx(__fmaf_rn(x[2 * i + 1], p.scale_log2, nbase));
         rs += e0 + e1;
         pk[i] = pack_bf16x2(e0, e1);
       }
@@ -382,13 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const uint32_t pcol = b ? L::kColP1 : L::kColP0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = pk[c * 8 + i];
-        tmem_st8(tmem + lane_addr + pcol + c * 8, w);
-      }
+      tmem_st32(tmem + lane_addr + pcol, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
