@@ -39,9 +39,11 @@ CONFIGS = {
     "phi3_window": "Phi-3-mini sliding-window layer, 32 rows, window 2047",
     "qwen3": "Qwen3-4B-shaped layer, 256 rows, QK-norm, shared prefix pages",
     "llama_step": "Llama-3.1-8B-shaped step_paged layer, 4x512 chunk tokens + 128 decode rows",
+    "llama_prefill": "Llama-3.1-8B-shaped prefill_paged layer, 4x1024 chunk tokens at offsets U[0,16384]",
 }
 METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and row-steps/sec per layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1700.0
 
 
 def algorithmic_bytes(w) -> dict:
@@ -87,6 +89,17 @@ def algorithmic_bytes(w) -> dict:
             "step": dec_kv + dec_q_out + dec_table + ch_kv + ch_q_out + append}
 
 
+def chunk_flops(w) -> int:
+    """Algorithmic flops of the chunk tokens' attention: for each token and q
+    head, a multiply-add per visible key and dimension for Q.K and for P.V."""
+    tot = 0
+    for p in w.ch_positions:
+        p = int(p)
+        lo = max(0, p - w.window + 1) if w.window else 0
+        tot += 4 * (p - lo + 1) * w.hq * w.head_dim
+    return tot
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -95,6 +108,18 @@ def read_peaks():
         return float(peaks["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_tensor_peak():
+    """Dense bf16 TFLOP/s: the sustained figure (kernels here run inside long
+    loops of steps)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (sustained)"
 
 
 def recorded_traffic(kernel_file: str, config: str):
@@ -174,9 +199,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(w, rows, repeats=1):
-    """Time the oracle (as it stands) on a sample of decode rows; returns
-    (seconds, algorithmic bytes of the sample, threads)."""
+def sample_tokens(w, n):
+    """A seeded sample of n step tokens: decode rows if the step has any, else
+    chunk tokens."""
+    rng = np.random.default_rng(0)
+    if w.B:
+        return sorted((w.P + rng.choice(w.B, size=min(w.B, n), replace=False)).tolist())
+    return sorted(rng.choice(w.P, size=min(w.P, n), replace=False).tolist())
+
+
+def cpu_oracle_sample(w, tokens, repeats=1):
+    """Time the oracle (as it stands) on a sample of step tokens: for each, the
+    append of the step tokens that write into the pages it reads, then its
+    attention; returns (seconds, algorithmic bytes of the sample)."""
     import synth  # noqa: F401
     from oracle import paged, rope
     sample = []
@@ -184,26 +219,34 @@ def cpu_oracle_sample(w, rows, repeats=1):
     inv = rope.inv_freq(w.theta, w.head_dim, w.llama3)
     q_all, k_all, v_all = w.step_q(), w.step_k(), w.step_v()
     gq, gk = w.gamma_q(), w.gamma_k()
-    for b in rows:
-        t = w.P + b
-        p = int(tp[t])
+    for t in tokens:
+        p, row = int(tp[t]), int(tr[t])
         lo = max(0, p - w.window + 1) if w.window else 0
         lps = np.arange(lo // 64, p // 64 + 1)
-        pages = w.table[b, lps]
+        pages = w.table[row, lps]
+        index = {int(pg): i for i, pg in enumerate(pages)}
         kp = np.stack([w.pool_pages("k", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
         vp = np.stack([w.pool_pages("v", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        writers, slots = [], []
+        for u in range(w.T):
+            pu = int(tp[u])
+            if pu < 0:
+                continue
+            pg = int(w.table[int(tr[u]), pu // 64])
+            if pg in index:
+                writers.append(u)
+                slots.append(index[pg] * 64 + pu % 64)
         ctable = np.full((1, lps[-1] + 1), -1, dtype=np.int32)
         ctable[0, lps] = np.arange(len(lps), dtype=np.int32)
-        slot = (len(lps) - 1) * 64 + p % 64
-        sample.append((t, p, kp, vp, ctable, slot, (p - lo + 1)))
+        sample.append((np.array(writers), np.array(slots), writers.index(t), p, kp, vp, ctable, p - lo + 1))
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(repeats):
-        for (t, p, kp, vp, ctable, slot, nkeys) in sample:
-            q_out, kp2, vp2 = paged.append_rope(q_all[[t]], k_all[[t]], v_all[[t]], tp[[t]], tr[[t]], None,
-                                                kp, vp, inv, slots=np.array([slot]), gamma_q=gq,
+        for (wi, slots, me, p, kp, vp, ctable, nkeys) in sample:
+            q_out, kp2, vp2 = paged.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None,
+                                                kp, vp, inv, slots=slots, gamma_q=gq,
                                                 gamma_k=gk, eps=w.norm_eps)
-            paged.attention_at(q_out[0], 0, p, ctable, kp2, vp2, w.window)
+            paged.attention_at(q_out[me], 0, p, ctable, kp2, vp2, w.window)
             nbytes += 2 * w.hkv * nkeys * w.head_dim * 2 + 2 * w.hq * w.head_dim * 2
     return time.perf_counter() - t0, nbytes
 
@@ -223,8 +266,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = synth.build(args.config, scale=args.scale, rows=args.rows)
-    rng = np.random.default_rng(0)
-    rows = sorted(rng.choice(w.B, size=min(w.B, args.ref_rows), replace=False).tolist())
+    rows = sample_tokens(w, args.ref_rows)
     for _ in range(max(0, args.warmup)):
         cpu_oracle_sample(w, rows[:1])
     secs, nbytes = 0.0, 0
@@ -242,7 +284,8 @@ def run_reference(args, rank, world):
         "config": {"workload": args.config, "description": CONFIGS[args.config],
                    "sample_rows_per_step": len(rows)},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{len(rows)} decode rows of the {args.config} workload per step"},
+                         "sample": f"{len(rows)} {'decode rows' if w.B else 'chunk tokens'} of the "
+                                   f"{args.config} workload per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
@@ -258,8 +301,7 @@ def run_gpu(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    seed = None if rank == 0 else 1000 + 97 * rank + {"phi3_tiny": 1, "mistral": 2, "phi3_window": 3,
-                                                       "qwen3": 4, "llama_step": 5}[args.config]
+    seed = None if rank == 0 else 1000 + 97 * rank + synth.WORKLOADS[args.config]
     w = synth.build(args.config, seed=seed, scale=args.scale, rows=args.rows)
     parts = algorithmic_bytes(w)
     pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * 2
@@ -418,8 +460,25 @@ def run_gpu(args, rank, world, dist):
     value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
     e2e_value = world * step_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9
     dec_bytes = parts["decode_call"] + (parts["chunk_kv"] + parts["chunk_q_out"] if w.P else 0)
-    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic("decode.cu", args.config)
+    if w.B:  # decode rows dominate: HBM bound
+        achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm",
+                    "kernel": ("lnk_paged_step_attn (chunk_kernel + decode_kernel)" if w.P
+                               else "lnk_paged_decode_attn (decode_kernel)"),
+                    "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                    "traffic": recorded_traffic("decode.cu", args.config), "algorithmic_bytes": dec_bytes}
+    else:  # prefill alone: the chunk kernel's contractions, tensor bound
+        flops = chunk_flops(w)
+        tpeak, tkind = read_tensor_peak()
+        achieved = flops / (dec_avg_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "lnk_paged_step_attn (chunk_kernel)",
+                    "achieved": round(achieved, 2), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(achieved / tpeak, 4), "peak_source": tkind,
+                    "traffic": recorded_traffic("chunk.cu", args.config), "algorithmic_flops": flops}
+    roofline["avg_launch_ms"] = round(dec_avg_ms, 5)
+    roofline["timing"] = (f"CUDA events around the attention call on its stream, {kt_steps} steps "
+                          "of the same workload right after the timed region")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -433,22 +492,16 @@ def run_gpu(args, rank, world, dist):
                          "alternated step to step",
                    "algorithmic_bytes_per_step": step_bytes},
         "row_steps_per_s": round(world * w.B * args.steps / (elapsed_ms / 1e3), 1),
+        "chunk_tokens_per_s": round(world * w.P * args.steps / (elapsed_ms / 1e3), 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": ("lnk_paged_step_attn (chunk_kernel + decode_kernel)" if w.P else "lnk_paged_decode_attn (decode_kernel)"),
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes": dec_bytes,
-                     "avg_launch_ms": round(dec_avg_ms, 5),
-                     "timing": f"CUDA events around the attention call on its stream, {kt_steps} steps "
-                               "of the same workload right after the timed region"},
+        "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        rng = np.random.default_rng(0)
-        rows_s = sorted(rng.choice(w.B, size=min(w.B, args.ref_rows), replace=False).tolist())
+        rows_s = sample_tokens(w, args.ref_rows)
         secs, nb, reps = 0.0, 0, 0
         while secs < args.cpu_seconds and reps < 50:
             s, b = cpu_oracle_sample(w, rows_s)
@@ -457,8 +510,8 @@ def run_gpu(args, rank, world, dist):
             reps += 1
         line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": threads_used(),
                                 "kind": "oracle",
-                                "sample": f"{len(rows_s)} decode rows x {reps} repeats of the {args.config} "
-                                          f"workload ({secs:.1f} s)"}
+                                "sample": f"{len(rows_s)} {'decode rows' if w.B else 'chunk tokens'} x {reps} "
+                                          f"repeats of the {args.config} workload ({secs:.1f} s)"}
     return line
 
 

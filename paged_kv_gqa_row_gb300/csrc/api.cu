@@ -49,25 +49,6 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const lnk_attn_desc& d) {
   return r == CUDA_SUCCESS;
 }
 
-// Tensor map over the chunk tokens' queries [P][Hq][D] as a 3-D tensor
-// (D, Hq, P): one box is 64 columns x G heads x tile_tokens tokens, i.e. the
-// 128 query rows of a chunk tile for one kv head, 128-byte swizzle.
-bool make_query_map(CUtensorMap* map, const void* q, const lnk_attn_desc& d, int P, int tile_tokens) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const int G = d.num_q_heads / d.num_kv_heads;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d.head_dim), static_cast<cuuint64_t>(d.num_q_heads),
-                        static_cast<cuuint64_t>(P)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d.head_dim) * 2,
-                           static_cast<cuuint64_t>(d.num_q_heads) * d.head_dim * 2};
-  cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tile_tokens)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shape checks shared by every entry point.
@@ -310,11 +291,9 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
     c.pages_per_row = desc->pages_per_row;
     c.window = desc->window;
     c.tile_tokens = 128 / group;
-    c.num_tiles = (P + c.tile_tokens - 1) / c.tile_tokens;
+    c.num_tiles = (P + kChunkHalves * c.tile_tokens - 1) / (kChunkHalves * c.tile_tokens);
     c.scale_log2 = scale_log2(desc);
-    CUtensorMap qmap;
-    if (!make_query_map(&qmap, q_roped, *desc, P, c.tile_tokens)) return LNK_ECUDA;
-    if (launch_chunk(qmap, kmap, vmap, c, desc->head_dim, s) != cudaSuccess) return LNK_ECUDA;
+    if (launch_chunk(kmap, vmap, c, desc->head_dim, s) != cudaSuccess) return LNK_ECUDA;
   }
   if (B > 0) {
     st = decode_common(desc, q_roped + static_cast<size_t>(P) * row_elems, step_positions, table, k_pool, v_pool,

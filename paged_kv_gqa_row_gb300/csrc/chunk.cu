@@ -3,29 +3,34 @@
 //
 // Every chunk token attends over its own row's pages up to its position (and
 // the window).  A CTA takes one tile of consecutive pack tokens and one kv
-// head: tile_tokens = 128 / G tokens times the G query heads of that kv head
-// gives 128 query rows (row m = token * G + head), one tensor-memory lane each.
-// Tokens of a tile are grouped into runs of equal table rows; for each run the
-// pages covering the run's key range are streamed through the kernel.
+// head: 256 / G tokens times the G query heads of that kv head, i.e. 256
+// query rows (row m = token * G + head) in two halves of 128 rows; each half
+// owns the 128 tensor-memory lanes in its own 256 columns.  Tokens of a tile
+// are grouped into runs of equal table rows; for each run the pages covering
+// the run's key range are streamed through the kernel once, for both halves.
 //
-// CTA structure (192 threads, warp-specialised):
-//  * warp 0, producer: loads the tile's queries once (3-D TMA box of
-//    tokens x G heads x 64 columns) and each page's K and V (2-D TMA boxes,
-//    128-byte swizzle) into a ring of stages;
-//  * warp 1, MMA: one thread issues, per page j,
-//      S_j[128 x 64]  = Q K_j^T          (tcgen05.mma, both operands in shared
-//                                         memory, K-major; S double-buffered in
-//                                         tensor memory)
-//      O[128 x D]    += P_j V_j          (P_j from tensor memory as bf16, V_j
-//                                         MN-major in shared memory)
-//    S_{j+1} is issued before P_j V_j so that the tensor core works while the
-//    softmax handles page j; commits release stages and signal the softmax;
-//  * warps 2-5, softmax: thread r owns query row r (tensor-memory lane r):
-//    reads its 64 scores, masks them (same run, lo <= key <= position),
-//    updates the running max and sum in registers, writes P_j back to tensor
-//    memory, and rescales its row of O only when the running max grows by more
-//    than 2^8 (until then P stays below 256, exact enough in bf16); at the end
-//    it normalises its row of O and stores it.
+// CTA structure (320 threads, warp-specialised):
+//  * warp 0, producer: loads each page's K and V (2-D TMA boxes, 128-byte
+//    swizzle) into a ring of stages;
+//  * warp 1, MMA: one thread issues, per page j and half h,
+//      S_h[128 x 64]  = Q_h K_j^T        (tcgen05.mma; Q_h from tensor memory,
+//                                         K_j K-major in shared memory)
+//      O_h[128 x D]  += P_h V_j          (P from tensor memory as bf16, written
+//                                         over the first 32 columns of S_h;
+//                                         V_j MN-major in shared memory)
+//    in the order P.V of half 0, Q.K of half 0 for the next page, then the
+//    same for half 1: while the softmax of one half works on a page the
+//    tensor core serves the other half (ping-pong).  The products issued by
+//    one thread run in order, so Q.K of the next page overwrites S_h only
+//    after P.V has read P from it.  With Q in tensor memory a Q.K product
+//    reads only K from shared memory;
+//  * warps 2-9, softmax, four per half: thread r of a half owns query row r
+//    (tensor-memory lane r).  It first writes its query row into tensor
+//    memory; then, per page, it reads its 64 scores, masks them (same run,
+//    lo <= key <= position), updates the running max and sum in registers,
+//    writes P back to tensor memory, and rescales its row of O only when the
+//    running max grows by more than 2^8 (until then P stays below 256, exact
+//    enough in bf16); at the end it normalises its row of O and stores it.
 //
 // Sources: "Mistral 7B Instruct v0.3", Entries table (prefill_paged: prompts
 // packed end to end, each token written at its place in the pool and attending
@@ -38,10 +43,13 @@
 namespace lnk {
 namespace {
 
-constexpr int kThreads = 6 * 32;
-constexpr int kStages = 3;
-constexpr int kRows = 128;               // query rows per tile = tensor-memory lanes
-constexpr float kRescaleLog2 = 8.f;      // rescale O when the max grows by more than 2^8
+constexpr int kHalves = kChunkHalves;
+constexpr int kSoftmaxWarps = 4 * kHalves;
+constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
+constexpr int kStages = 4;
+constexpr int kRows = 128;                // query rows per half = tensor-memory lanes
+constexpr int kTileRows = kRows * kHalves;
+constexpr float kRescaleLog2 = 8.f;       // rescale O when the max grows by more than 2^8
 
 struct PageInfo {
   int run, key_base, valid, pad;
@@ -50,29 +58,29 @@ struct PageInfo {
 template <int D>
 struct TcSmem {
   static constexpr int NB = boxes_for(D);
-  static constexpr int kQBytes = NB * kRows * 128;          // query tile: NB boxes of 128 rows x 128 B
   static constexpr int kStageBytes = 2 * NB * kBoxBytes;    // K boxes, then V boxes
   static constexpr int kPvN = D <= 64 ? 64 : 128;           // N of the P.V product (D = 96 padded)
-  static constexpr uint32_t kTmemCols = D <= 64 ? 256 : 512;
-  // tensor-memory columns
-  static constexpr uint32_t kColS0 = 0, kColS1 = 64, kColP0 = 128, kColP1 = 160, kColO = 192;
-  static constexpr size_t q = 0;
-  static constexpr size_t stages = q + kQBytes;
+  static constexpr uint32_t kTmemCols = 512;
+  // tensor-memory columns of a half (half h adds h * kHalfCols): Q (bf16
+  // pairs), S (P of the page over its first 32 columns), O
+  static constexpr uint32_t kHalfCols = 256;
+  static constexpr uint32_t kColQ = 0, kColS = 64, kColO = 128;
+  static constexpr size_t stages = 0;
   static constexpr size_t bars = stages + size_t(kStages) * kStageBytes;
-  // full[S], empty[S], q_full, s_full[2], p_full[2], pv_done[2], zero
-  static constexpr int kNumBars = 2 * kStages + 8;
+  // full[S], empty[S], q_full, s_full[H], p_full[H], pv_done[H], zero
+  static constexpr int kNumBars = 2 * kStages + 2 + 3 * kHalves;
   static constexpr size_t info = bars + kNumBars * sizeof(uint64_t);
   static constexpr size_t tok = info + kStages * sizeof(PageInfo);
-  static constexpr size_t runs = tok + 3 * kRows * 4;
-  static constexpr size_t misc = runs + 4 * kRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base
-  // at least 100 KiB so that no more CTAs share an SM than its tensor memory holds
-  static constexpr size_t bytes = (misc + 64 + 1024) > 102400 ? (misc + 64 + 1024) : 102400;
+  static constexpr size_t runs = tok + 4 * kTileRows * 4;
+  static constexpr size_t misc = runs + 4 * kTileRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base
+  // more than half of the shared memory, so that one CTA holds the tensor memory of an SM
+  static constexpr size_t bytes = (misc + 64 + 1024) > 120 * 1024 ? (misc + 64 + 1024) : 120 * 1024;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                 const __grid_constant__ CUtensorMap vmap, const ChunkParams p) {
+    chunk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                 const ChunkParams p) {
   using L = TcSmem<D>;
   constexpr int NB = L::NB;
   constexpr int DK = D / 16;
@@ -81,18 +89,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* q_full = empty_bar + kStages;
-  uint64_t* s_full = q_full + 1;    // [2]
-  uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* pv_done = p_full + 2;   // [2]
-  uint64_t* zero_bar = pv_done + 2;
+  uint64_t* s_full = q_full + 1;          // [H]
+  uint64_t* p_full = s_full + kHalves;    // [H]
+  uint64_t* pv_done = p_full + kHalves;   // [H]
+  uint64_t* zero_bar = pv_done + kHalves;
   PageInfo* info = reinterpret_cast<PageInfo*>(smem + L::info);
   int* tok_lo = reinterpret_cast<int*>(smem + L::tok);
-  int* tok_hi = tok_lo + kRows;
-  int* tok_run = tok_hi + kRows;
+  int* tok_hi = tok_lo + kTileRows;
+  int* tok_run = tok_hi + kTileRows;
+  int* tok_row = tok_run + kTileRows;
   int* run_row = reinterpret_cast<int*>(smem + L::runs);
-  int* run_kmin = run_row + kRows;
-  int* run_kmax = run_kmin + kRows;
-  int* run_pages = run_kmax + kRows;
+  int* run_kmin = run_row + kTileRows;
+  int* run_kmax = run_kmin + kTileRows;
+  int* run_pages = run_kmax + kTileRows;
   int* misc = reinterpret_cast<int*>(smem + L::misc);
   volatile int* abort_flag = misc + 2;
 
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int G = p.group;
-  const int TQ = p.tile_tokens;
+  const int TQ = kHalves * p.tile_tokens;  // tokens of the tile
   const int tile = p.num_tiles - 1 - static_cast<int>(blockIdx.x);  // later tokens first
   const int h = blockIdx.y;
   const int t0 = tile * TQ;
@@ -111,24 +120,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(full_bar + s), 1);
       mbar_init(smem_addr(empty_bar + s), 1);
     }
-    mbar_init(smem_addr(q_full), 1);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(smem_addr(q_full), kSoftmaxWarps);
+    for (int i = 0; i < kHalves; ++i) {
       mbar_init(smem_addr(s_full + i), 1);
       mbar_init(smem_addr(p_full + i), 4);
       mbar_init(smem_addr(pv_done + i), 1);
     }
-    mbar_init(smem_addr(zero_bar), kRows);
+    mbar_init(smem_addr(zero_bar), kTileRows);
     misc[2] = 0;
     fence_mbarrier_init();
   }
   if (warp == 1) tmem_alloc(smem_addr(misc + 3), L::kTmemCols);
   // ---- tokens of the tile ----
   if (tid < TQ) {
-    int lo = 0, hi = 0, bad = 0;
+    int lo = 0, hi = 0, bad = 0, row = -1;
     if (tid < nt) {
       const int t = t0 + tid;
       const int pos = p.positions[t];
-      const int row = p.rows[t];
+      row = p.rows[t];
       if (pos >= 0) {
         if (row < 0 || row >= p.num_rows) bad = LNK_DEV_BAD_ROW;
         else if (pos >= p.pages_per_row * kPage) bad = LNK_DEV_BAD_POSITION;
@@ -143,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tok_lo[tid] = lo;
     tok_hi[tid] = hi;
+    tok_row[tid] = row;
     if (bad && h == 0 && p.status != nullptr) atomicOr(p.status, bad);
   }
   __syncthreads();
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tok_run[i] = -1;
         continue;
       }
-      const int row = p.rows[t0 + i];
+      const int row = tok_row[i];
       if (cur < 0 || run_row[cur] != row) {
         cur = nr++;
         run_row[cur] = row;
@@ -183,12 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ============================== producer ==============================
     if (lane == 0 && npages > 0) {
-      tma_prefetch_descriptor(&qmap);
-      const uint32_t qb = smem_addr(q_full);
-      mbar_arrive_expect_tx(qb, L::kQBytes);
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-        tma_load_3d(smem_addr(smem + L::q + nb * kRows * 128), &qmap, nb * kBoxCols, h * G, t0, qb);
       int k = 0;
       bool stop = false;
       for (int run = 0; run < nruns && !stop; ++run) {
@@ -237,61 +241,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && npages > 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(kRows, 64, 0, 0);
       constexpr uint32_t kIdPV = umma_idesc_bf16(kRows, L::kPvN, 0, 1);
-      const uint32_t qaddr = smem_addr(smem + L::q);
-      bool ok = mbar_wait(smem_addr(q_full), 0, abort_flag);
-      tc_fence_after();
-      int last_pv = -1;
-      for (int j = 0; ok && j <= npages; ++j) {
-        if (j < npages) {
-          const int s = j % kStages, b = j & 1;
-          if (!mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t kaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+      // S_hf = Q_hf K^T for the page in stage s (Q from tensor memory)
+      auto issue_s = [&](int hf, int s) {
+        const uint32_t kaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+        const uint32_t hc = tmem + hf * L::kHalfCols;
 #pragma unroll
-          for (int kk = 0; kk < DK; ++kk) {
-            const uint64_t ad = umma_desc_sw128(qaddr + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 0, 1024);
-            const uint64_t bd = umma_desc_sw128(kaddr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 0, 1024);
-            umma_ss(tmem + (b ? L::kColS1 : L::kColS0), ad, bd, kIdS, kk > 0);
-          }
-          umma_commit(smem_addr(s_full + b));
+        for (int kk = 0; kk < DK; ++kk) {
+          const uint64_t bd = umma_desc_sw128(kaddr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 0, 1024);
+          umma_ts(hc + L::kColS, hc + L::kColQ + kk * 8, bd, kIdS, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % kStages, b = jj & 1;
-          if (!mbar_wait(smem_addr(p_full + b), (jj >> 1) & 1, abort_flag)) break;
+        umma_commit(smem_addr(s_full + hf));
+      };
+      bool ok = mbar_wait(smem_addr(q_full), 0, abort_flag) && mbar_wait(smem_addr(full_bar), 0, abort_flag);
+      tc_fence_after();
+      if (ok) {
+#pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf) issue_s(hf, 0);
+      }
+      int last_pv = -1;
+      for (int j = 0; ok && j < npages; ++j) {
+        const int s = j % kStages;
+        const uint32_t vaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes) + NB * kBoxBytes;
+#pragma unroll
+        for (int hf = 0; hf < kHalves && ok; ++hf) {
+          ok = mbar_wait(smem_addr(p_full + hf), j & 1, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t vaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes) + NB * kBoxBytes;
+          const uint32_t hc = tmem + hf * L::kHalfCols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 64 keys, 16 per instruction
             const uint64_t bd = umma_desc_sw128(vaddr + kk * 16 * 128, kBoxBytes, 1024);
-            umma_ts(tmem + L::kColO, tmem + (b ? L::kColP1 : L::kColP0) + kk * 8, bd, kIdPV, (jj > 0 || kk > 0));
+            umma_ts(hc + L::kColO, hc + L::kColS + kk * 8, bd, kIdPV, (j > 0 || kk > 0));
           }
-          umma_commit(smem_addr(empty_bar + s));
-          umma_commit(smem_addr(pv_done + b));
-          last_pv = jj;
+          umma_commit(smem_addr(pv_done + hf));
+          if (hf == kHalves - 1) {
+            umma_commit(smem_addr(empty_bar + s));
+            last_pv = j;
+          }
+          if (j + 1 < npages) {
+            const int s1 = (j + 1) % kStages;
+            if (hf == 0) {
+              ok = mbar_wait(smem_addr(full_bar + s1), ((j + 1) / kStages) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(hf, s1);
+          }
         }
       }
-      // the tensor memory is freed at the end: let the last product finish
+      // the tensor memory is freed at the end: let the last products finish
       if (last_pv >= 0) {
-        const uint32_t bar = smem_addr(pv_done + (last_pv & 1));
-        const uint64_t t_0 = global_timer_ns();
-        while (!mbar_try_wait(bar, (last_pv >> 1) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+        for (int hf = 0; hf < kHalves; ++hf) {
+          const uint32_t bar = smem_addr(pv_done + hf);
+          const uint64_t t_0 = global_timer_ns();
+          while (!mbar_try_wait(bar, last_pv & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+          }
         }
       }
     }
   } else {
     // ============================== softmax ===============================
+    const int hf = (warp - 2) / 4;        // half of the tile
     const int qt = warp & 3;              // tensor-memory lane quarter of this warp
-    const int row = qt * 32 + lane;       // query row = token * G + head
+    const int row = hf * kRows + qt * 32 + lane;  // query row of the tile = token * G + head
     const int tl = row / G, g = row % G;
     const int lo = tok_lo[tl], hi = tok_hi[tl], run_id = tok_run[tl];
     const bool live = tl < nt && run_id >= 0;
-    const uint32_t lane_addr = static_cast<uint32_t>(qt * 32) << 16;
-    const int ctid = tid - 64;            // 0..127 among the softmax threads
+    const uint32_t hcol = tmem + (static_cast<uint32_t>(qt * 32) << 16) + hf * L::kHalfCols;
+    const int ctid = tid - 64;            // 0..255 among the softmax threads
+    const size_t qrow = (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
+    // ---- this row's query into tensor memory (bf16 pairs, the A operand of Q.K) ----
+    if (npages > 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {  // 8 bf16 pairs = two 16-byte loads per step
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        if (tl < nt) {
+          a = src[2 * c];
+          b = src[2 * c + 1];
+        }
+        const uint32_t r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        tmem_st8(hcol + L::kColQ + c * 8, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(q_full));
+    }
     float m_ref = -INFINITY, l_sum = 0.f;
     uint32_t zero_uses = 0;
     bool ok = true;
     for (int j = 0; j < npages && ok; ++j) {
-      const int s = j % kStages, b = j & 1;
+      const int s = j % kStages;
       ok = mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag);
       if (!ok) break;
       const PageInfo si = info[s];
@@ -300,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Keys of this page outside the run's range may hold stale or
         // uninitialised data: zero their value rows before P.V reads them.
         uint8_t* vb = smem + L::stages + size_t(s) * L::kStageBytes + NB * kBoxBytes;
-        for (int i = ctid; i < kPage * NB * 8; i += kRows) {
+        for (int i = ctid; i < kPage * NB * 8; i += kTileRows) {
           const int key = i / (NB * 8), rest = i % (NB * 8);
           if (!si.valid || si.key_base + key < kmin || si.key_base + key >= kmax)
             *reinterpret_cast<uint4*>(vb + (rest >> 3) * kBoxBytes + key * 128 + (rest & 7) * 16) =
@@ -312,14 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++zero_uses;
       }
       if (!ok) break;
-      ok = mbar_wait(smem_addr(s_full + b), (j >> 1) & 1, abort_flag);
+      ok = mbar_wait(smem_addr(s_full + hf), j & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
       float x[64];
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + lane_addr + (b ? L::kColS1 : L::kColS0), r0);
-        tmem_ld32(tmem + lane_addr + (b ? L::kColS1 : L::kColS0) + 32, r1);
+        tmem_ld32(hcol + L::kColS, r0);
+        tmem_ld32(hcol + L::kColS + 32, r1);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -331,17 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_run = live && si.valid && si.run == run_id;
       const int ka = in_run ? max(lo - si.key_base, 0) : kPage;
       const int ke = in_run ? max(ka, min(hi - si.key_base, kPage)) : kPage;
-      float mraw = -INFINITY;
-      if (__all_sync(0xffffffffu, ka == 0 && ke == kPage)) {
+      if (!__all_sync(0xffffffffu, ka == 0 && ke == kPage)) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, x[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = (i >= ka && i < ke) ? x[i] : -INFINITY;
-          mraw = fmaxf(mraw, x[i]);
-        }
+        for (int i = 0; i < 64; ++i) x[i] = (i >= ka && i < ke) ? x[i] : -INFINITY;
       }
+      // row max as a tree of independent maxima
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(x[i], x[i + 8]);
+#pragma unroll
+      for (int i = 16; i < 64; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], x[i + k]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;  // log2 units
       // running max: rescale O only when it grows by more than 2^8
       float alpha = 1.f;
@@ -355,58 +399,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__any_sync(0xffffffffu, alpha != 1.f) && j >= 1) {
-        const int jp = j - 1;
-        ok = mbar_wait(smem_addr(pv_done + (jp & 1)), (jp >> 1) & 1, abort_flag);
+        ok = mbar_wait(smem_addr(pv_done + hf), (j - 1) & 1, abort_flag);  // P.V of page j - 1
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < L::kPvN / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + L::kColO + c * 32, r);
+          tmem_ld32(hcol + L::kColO + c * 32, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tmem + lane_addr + L::kColO + c * 32, r);
+          tmem_st32(hcol + L::kColO + c * 32, r);
         }
         tmem_st_wait();
       }
       // probabilities 2^(s * scale * log2(e) - m_ref), packed to bf16
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       uint32_t pk[32];
-      float rs = 0.f;
+      float r8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) r8[k] = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float e0 = ex2_approx(__fmaf_rn(x[2 * i], p.scale_log2, nbase));
         const float e1 = ex2_approx(__fmaf_rn(x[2 * i + 1], p.scale_log2, nbase));
-        rs += e0 + e1;
+        r8[i & 7] += e0 + e1;
         pk[i] = pack_bf16x2(e0, e1);
       }
-      l_sum += rs;
-      if (j >= 2) {  // P buffer b was last read by P.V of page j - 2
-        ok = mbar_wait(smem_addr(pv_done + b), ((j - 2) >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      const uint32_t pcol = b ? L::kColP1 : L::kColP0;
-      tmem_st32(tmem + lane_addr + pcol, pk);
+      l_sum += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+      tmem_st32(hcol + L::kColS, pk);  // P over the scores just read
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_full + b));
+      if (lane == 0) mbar_arrive(smem_addr(p_full + hf));
     }
     // ---- normalise and store this row ----
     if (ok && npages > 0) {
-      const int jl = npages - 1;
-      ok = mbar_wait(smem_addr(pv_done + (jl & 1)), (jl >> 1) & 1, abort_flag);
+      ok = mbar_wait(smem_addr(pv_done + hf), (npages - 1) & 1, abort_flag);
       tc_fence_after();
     }
-    uint16_t* dst = p.out + (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
+    uint16_t* dst = p.out + qrow;
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
 #pragma unroll 1
     for (int c = 0; c < L::kPvN / 16; ++c) {
       uint32_t r[16];
       if (ok && npages > 0) {
-        tmem_ld16(tmem + lane_addr + L::kColO + c * 16, r);
+        tmem_ld16(hcol + L::kColO + c * 16, r);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -433,14 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_chunk_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const ChunkParams& p, cudaStream_t stream) {
+cudaError_t launch_chunk_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
+                           cudaStream_t stream) {
   const int bytes = static_cast<int>(TcSmem<D>::bytes);
   cudaError_t err =
       cudaFuncSetAttribute(chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_tiles, p.hkv);
-  chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(qmap, kmap, vmap, p);
+  chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
@@ -456,13 +494,13 @@ __global__ void gather_last_kernel(const uint16_t* out, const int32_t* last, uin
 
 }  // namespace
 
-cudaError_t launch_chunk(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         const ChunkParams& p, int head_dim, cudaStream_t stream) {
+cudaError_t launch_chunk(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p, int head_dim,
+                         cudaStream_t stream) {
   if (p.P == 0) return cudaSuccess;
   switch (head_dim) {
-    case 64: return launch_chunk_t<64>(qmap, kmap, vmap, p, stream);
-    case 96: return launch_chunk_t<96>(qmap, kmap, vmap, p, stream);
-    case 128: return launch_chunk_t<128>(qmap, kmap, vmap, p, stream);
+    case 64: return launch_chunk_t<64>(kmap, vmap, p, stream);
+    case 96: return launch_chunk_t<96>(kmap, vmap, p, stream);
+    case 128: return launch_chunk_t<128>(kmap, vmap, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -70,6 +70,9 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
                           int head_dim, const DecodeLaunch& launch, cudaStream_t stream);
 
 // ----------------------------------------------------------------- chunk --
+// A chunk-attention CTA holds this many halves of 128 query rows.
+constexpr int kChunkHalves = 2;
+
 struct ChunkParams {
   const uint16_t* q;          // [P][Hq][D]
   const int32_t* rows;        // [P]
@@ -79,12 +82,12 @@ struct ChunkParams {
   uint16_t* out;              // [P][Hq][D]
   int32_t* status;
   int P, hq, hkv, group, num_pages, num_rows, pages_per_row, window;
-  int tile_tokens, num_tiles;
+  int tile_tokens, num_tiles;  // tokens per half tile (128 / group); tiles of kChunkHalves halves
   float scale_log2;
 };
 
-cudaError_t launch_chunk(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         const ChunkParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_chunk(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p, int head_dim,
+                         cudaStream_t stream);
 
 // ------------------------------------------------------------ gather last --
 cudaError_t launch_gather_last(const uint16_t* out, const int32_t* last, uint16_t* last_out, int M,

@@ -246,6 +246,11 @@ def _pages_for(last_position: int) -> int:
     return last_position // PAGE_SIZE + 1
 
 
+# workload name -> index (the default seed of workload k is 1000 + k)
+WORKLOADS = {"phi3_tiny": 1, "mistral": 2, "phi3_window": 3, "qwen3": 4, "llama_step": 5,
+             "llama_prefill": 6}
+
+
 def build(name: str, seed: Optional[int] = None, scale: float = 1.0,
           rows: Optional[int] = None) -> Workload:
     """Build one of the five named workloads.
@@ -253,7 +258,7 @@ def build(name: str, seed: Optional[int] = None, scale: float = 1.0,
     ``scale`` (<= 1) shrinks context lengths (and chunk offsets) for small
     parity cases; ``rows`` overrides the number of decode rows.
     """
-    idx = {"phi3_tiny": 1, "mistral": 2, "phi3_window": 3, "qwen3": 4, "llama_step": 5}[name]
+    idx = WORKLOADS[name]
     if seed is None:
         seed = 1000 + idx
     rng = np.random.default_rng(seed)
@@ -320,11 +325,15 @@ def build(name: str, seed: Optional[int] = None, scale: float = 1.0,
         return Workload(name, seed, 32, 8, 128, 1e6, None, 0, True, total, table, pos,
                         empty, empty, empty, dump_page=dump)
 
-    if name == "llama_step":
-        B = rows if rows is not None else 128
+    if name in ("llama_step", "llama_prefill"):
+        # llama_step: 128 decode rows plus 4 chunks of 512 tokens;
+        # llama_prefill: prefill alone, 4 chunks of 1024 tokens (4096 tokens)
+        step = name == "llama_step"
+        B = rows if rows is not None else (128 if step else 0)
         L = rng.integers(scaled(1024, 2), scaled(131072, 3) + 1, size=B)
         pos = (L - 1).astype(np.int32)
-        n_chunks, chunk = 4, (512 if scale >= 1.0 else max(8, scaled(512, 8)))
+        full = 512 if step else 1024
+        n_chunks, chunk = 4, (full if scale >= 1.0 else max(8, scaled(full, 8)))
         offsets = rng.integers(0, scaled(16384, 1) + 1, size=n_chunks)
         need = [_pages_for(int(p)) for p in pos]
         need += [_pages_for(int(o) + chunk - 1) for o in offsets]

@@ -197,26 +197,32 @@ def test_inv_freq_table_matches_oracle():
 
 # ------------------------------------------------------------- workloads ----
 
-@pytest.mark.parametrize("name", ["phi3_tiny", "mistral", "phi3_window", "qwen3", "llama_step"])
+@pytest.mark.parametrize("name", ["phi3_tiny", "mistral", "phi3_window", "qwen3", "llama_step", "llama_prefill"])
 def test_workload_scaled_down(name):
-    scale = {"phi3_tiny": 1.0, "mistral": 0.06, "phi3_window": 0.6, "qwen3": 0.05, "llama_step": 0.02}[name]
-    rows = {"phi3_tiny": None, "mistral": 12, "phi3_window": 8, "qwen3": 40, "llama_step": 6}[name]
+    scale = {"phi3_tiny": 1.0, "mistral": 0.06, "phi3_window": 0.6, "qwen3": 0.05, "llama_step": 0.02,
+             "llama_prefill": 0.03}[name]
+    rows = {"phi3_tiny": None, "mistral": 12, "phi3_window": 8, "qwen3": 40, "llama_step": 6,
+            "llama_prefill": None}[name]
     w = synth.build(name, scale=scale, rows=rows)
     _check_full(w)
 
 
 def _sample_tokens(w, n_dec=6, per_chunk=2):
-    order = np.argsort(w.dec_positions)
-    picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])} |
-                   {int(x) for x in np.linspace(0, w.B - 1, max(0, n_dec - 3)).astype(int)})
-    toks = [w.P + b for b in picks]
+    toks = []
+    if w.B:
+        order = np.argsort(w.dec_positions)
+        picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])} |
+                       {int(x) for x in np.linspace(0, w.B - 1, max(0, n_dec - 3)).astype(int)})
+        toks = [w.P + b for b in picks]
     for c in np.unique(w.ch_segments):
         idx = np.nonzero(w.ch_segments == c)[0]
-        toks += [int(idx[0]), int(idx[-1])][:per_chunk]
+        # first, last, and (for long chunks) a token inside: a tile boundary and a ragged one
+        extra = [int(idx[len(idx) // 2]), int(idx[min(len(idx) - 1, 130)])] if per_chunk > 2 else []
+        toks += ([int(idx[0]), int(idx[-1])] + extra)[:per_chunk]
     return toks
 
 
-@pytest.mark.parametrize("name", ["mistral", "phi3_window", "qwen3", "llama_step"])
+@pytest.mark.parametrize("name", ["mistral", "phi3_window", "qwen3", "llama_step", "llama_prefill"])
 def test_workload_full_size_sampled(name):
     """Full-size workloads in the bench's launch configuration, checked on sampled tokens."""
     w = synth.build(name)
@@ -227,7 +233,7 @@ def test_workload_full_size_sampled(name):
     out = to_bits(dev.out)
     from oracle import bf16
     assert np.all(np.isfinite(bf16.to_f64(out)))
-    toks = _sample_tokens(w)
+    toks = _sample_tokens(w, per_chunk=4 if w.B == 0 else 2)
     want = oracle_tokens(w, toks)
     for t in toks:
         assert_attention_close(out[t], want[t], f"{name} token {t}")

@@ -35,7 +35,7 @@ def test_pool_pages_match_whole_pool():
 
 
 def test_workload_structure():
-    for name in ["phi3_tiny", "mistral", "phi3_window", "qwen3", "llama_step"]:
+    for name in sorted(synth.WORKLOADS):
         w = synth.build(name, scale=0.05)
         tp, tr = w.token_positions(), w.token_rows()
         assert len(tp) == w.T
