@@ -60,7 +60,8 @@ typedef enum lnk_status {
   LNK_ERANGE = 2,          /* a size outside the supported range */
   LNK_ECUDA = 3,           /* a CUDA runtime call failed (launch, attribute, ...) */
   LNK_EUNSUPPORTED = 4,    /* head_dim, group size or page size not supported */
-  LNK_EWORKSPACE = 5       /* workspace NULL or smaller than lnk_paged_workspace_size */
+  LNK_EWORKSPACE = 5,      /* workspace NULL or smaller than lnk_paged_workspace_size */
+  LNK_ENOSPACE = 6         /* the page allocator has too few free pages (or host memory ran out) */
 } lnk_status;
 
 /* Bits ORed into *dev_status by the kernels. */
@@ -237,6 +238,84 @@ lnk_status lnk_paged_decode_attn_static(const lnk_attn_desc* desc, const lnk_bf1
                                         const lnk_bf16* k_pool, const lnk_bf16* v_pool,
                                         lnk_bf16* out, int32_t B, int32_t* dev_status,
                                         lnk_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Host page allocator (lnk_pager) and page copies
+ *
+ * Source: "Mistral 7B Instruct v0.3", Entries table (prefill_paged): a token
+ * attends over its row's pages up to its position -- "chunks, shared
+ * prefixes", so rows may map the same physical pages for a common prefix.
+ * The pages do not say how pages are handed out; this allocator is the
+ * plainest one that supports that sharing:
+ *   - free pages are handed out lowest page number first;
+ *   - each page has a reference count = the number of table entries mapping it;
+ *   - fork maps a new row onto the pages of another row's prefix;
+ *   - before a token is written, prepare_append maps a fresh page for an
+ *     unmapped logical page, and moves a row that writes into a page mapped
+ *     more than once onto a fresh private page (copy on write): the caller
+ *     copies the old page into the new one with lnk_paged_copy_pages before
+ *     the append;
+ *   - release drops a row's pages; a page whose count reaches 0 is free.
+ * The pager holds host memory only (its table is exported into a caller
+ * buffer for upload to the device) and is not thread-safe: serialise the
+ * calls made on one pager.  Host pointers below are host memory.
+ * ------------------------------------------------------------------------- */
+typedef struct lnk_pager lnk_pager;
+
+/* A pager over num_pages pages for a table of num_rows x pages_per_row, all
+ * unmapped (-1).  *out receives the handle (NULL on error).  LNK_EINVAL for a
+ * non-positive size, LNK_ENOSPACE if host memory runs out. */
+lnk_status lnk_pager_create(int32_t num_pages, int32_t num_rows, int32_t pages_per_row, lnk_pager** out);
+
+/* Frees the pager (NULL is ignored). */
+void lnk_pager_destroy(lnk_pager* pager);
+
+/* Maps a fresh page to every unmapped logical page of `row` covering positions
+ * [0, length).  Mapped pages are left as they are (shared ones included).
+ * LNK_ERANGE if length > pages_per_row * 64; LNK_ENOSPACE (nothing changed) if
+ * the free pages do not suffice. */
+lnk_status lnk_pager_reserve(lnk_pager* pager, int32_t row, int32_t length);
+
+/* Maps the first ceil(length / 64) logical pages of the empty row dst_row onto
+ * src_row's pages (their counts + 1); src_row must have them mapped.  A shared
+ * partial last page is copied on the first write into it (prepare_append).
+ * LNK_EINVAL if dst_row is not empty, src_row lacks a page, or the rows are
+ * equal or out of range. */
+lnk_status lnk_pager_fork(lnk_pager* pager, int32_t src_row, int32_t dst_row, int32_t length);
+
+/* Prepares the n tokens (rows[t], positions[t]; host arrays) that the next
+ * lnk_paged_append_rope will write, in order: the first token of the batch
+ * that writes into a logical page maps a fresh page if it is unmapped, or
+ * moves the row onto a fresh page if the page is mapped by other rows too;
+ * each such move appends (old page, new page) to copy_src/copy_dst (host
+ * arrays of capacity n) and *num_copies counts them.  Negative positions are
+ * skipped.  LNK_EINVAL for a bad row, LNK_ERANGE for a position past the
+ * table row, LNK_ENOSPACE if the free pages do not suffice; on any error
+ * nothing changes. */
+lnk_status lnk_pager_prepare_append(lnk_pager* pager, const int32_t* rows, const int32_t* positions, int32_t n,
+                                    int32_t* copy_src, int32_t* copy_dst, int32_t* num_copies);
+
+/* Unmaps every page of `row`; pages whose count reaches 0 become free. */
+lnk_status lnk_pager_release(lnk_pager* pager, int32_t row);
+
+/* Writes the table, [num_rows][pages_per_row] int32 (-1 = unmapped), into the
+ * host buffer `table`. */
+lnk_status lnk_pager_table(const lnk_pager* pager, int32_t* table);
+
+/* Number of free pages (-1 for a NULL pager). */
+int32_t lnk_pager_free_pages(const lnk_pager* pager);
+
+/* Reference count of `page` (-1 for a NULL pager or a page out of range). */
+int32_t lnk_pager_refcount(const lnk_pager* pager, int32_t page);
+
+/* Copies pages src_pages[i] -> dst_pages[i] (device int32 arrays of n) in the
+ * K and V pools, every kv head (the copy on write of prepare_append).  A pair
+ * with a page outside [0, num_pages) is skipped and sets LNK_DEV_BAD_PAGE in
+ * *dev_status.  Pairs must not overlap (no page both a source and a target).
+ * Enqueued on `stream`; call it before the append that writes the pages. */
+lnk_status lnk_paged_copy_pages(const lnk_attn_desc* desc, lnk_bf16* k_pool, lnk_bf16* v_pool,
+                                const int32_t* src_pages, const int32_t* dst_pages, int32_t n,
+                                int32_t* dev_status, lnk_stream stream);
 
 #ifdef __cplusplus
 }

@@ -9,9 +9,11 @@ from .binding import (  # noqa: F401
     LIBRARY_PATH,
     AttnDesc,
     LnkError,
+    Pager,
     RopeDesc,
     attn_desc,
     lnk_paged_append_rope,
+    lnk_paged_copy_pages,
     lnk_paged_decode_attn,
     lnk_paged_decode_attn_static,
     lnk_paged_step_attn,

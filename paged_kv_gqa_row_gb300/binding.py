@@ -23,13 +23,15 @@ c_i32, c_f32, c_f64, c_size, c_vp = ctypes.c_int32, ctypes.c_float, ctypes.c_dou
 
 LNK_OK = 0
 STATUS_NAMES = {0: "LNK_OK", 1: "LNK_EINVAL", 2: "LNK_ERANGE", 3: "LNK_ECUDA",
-                4: "LNK_EUNSUPPORTED", 5: "LNK_EWORKSPACE"}
+                4: "LNK_EUNSUPPORTED", 5: "LNK_EWORKSPACE", 6: "LNK_ENOSPACE"}
 DEV_BAD_ROW, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_BAD_SLOT = 0x01, 0x02, 0x04, 0x08
 DEV_SEGMENT, DEV_BAD_LAST, DEV_TIMEOUT = 0x10, 0x20, 0x40
 
 EXPORTED = ["lnk_status_string", "lnk_rope_inv_freq", "lnk_paged_workspace_size",
             "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_step_attn",
-            "lnk_paged_decode_attn_static"]
+            "lnk_paged_decode_attn_static", "lnk_pager_create", "lnk_pager_destroy", "lnk_pager_reserve",
+            "lnk_pager_fork", "lnk_pager_prepare_append", "lnk_pager_release", "lnk_pager_table",
+            "lnk_pager_free_pages", "lnk_pager_refcount", "lnk_paged_copy_pages"]
 
 
 class LnkError(RuntimeError):
@@ -71,6 +73,27 @@ _lib.lnk_paged_step_attn.restype = ctypes.c_int
 _lib.lnk_paged_step_attn.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                      c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_size,
                                      c_vp, c_vp]
+_i32p = ctypes.POINTER(c_i32)
+_lib.lnk_pager_create.restype = ctypes.c_int
+_lib.lnk_pager_create.argtypes = [c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]
+_lib.lnk_pager_destroy.restype = None
+_lib.lnk_pager_destroy.argtypes = [c_vp]
+_lib.lnk_pager_reserve.restype = ctypes.c_int
+_lib.lnk_pager_reserve.argtypes = [c_vp, c_i32, c_i32]
+_lib.lnk_pager_fork.restype = ctypes.c_int
+_lib.lnk_pager_fork.argtypes = [c_vp, c_i32, c_i32, c_i32]
+_lib.lnk_pager_prepare_append.restype = ctypes.c_int
+_lib.lnk_pager_prepare_append.argtypes = [c_vp, _i32p, _i32p, c_i32, _i32p, _i32p, _i32p]
+_lib.lnk_pager_release.restype = ctypes.c_int
+_lib.lnk_pager_release.argtypes = [c_vp, c_i32]
+_lib.lnk_pager_table.restype = ctypes.c_int
+_lib.lnk_pager_table.argtypes = [c_vp, _i32p]
+_lib.lnk_pager_free_pages.restype = c_i32
+_lib.lnk_pager_free_pages.argtypes = [c_vp]
+_lib.lnk_pager_refcount.restype = c_i32
+_lib.lnk_pager_refcount.argtypes = [c_vp, c_i32]
+_lib.lnk_paged_copy_pages.restype = ctypes.c_int
+_lib.lnk_paged_copy_pages.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp]
 
 
 def attn_desc(num_q_heads, num_kv_heads, head_dim, num_pages, num_rows, pages_per_row,
@@ -156,6 +179,72 @@ def lnk_paged_step_attn(desc, q_roped, rows, positions, segments, step_positions
                                   _ptr(v_pool), _ptr(out), _ptr(last), _ptr(last_out), P, B, M,
                                   _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "lnk_paged_step_attn")
+
+
+def lnk_paged_copy_pages(desc, k_pool, v_pool, src_pages, dst_pages, n, dev_status=None, stream=None):
+    st = _lib.lnk_paged_copy_pages(ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(src_pages),
+                                   _ptr(dst_pages), n, _ptr(dev_status), _stream(stream))
+    _check(st, "lnk_paged_copy_pages")
+
+
+def _i32_array(values):
+    import numpy as np
+    a = np.ascontiguousarray(values, dtype=np.int32)
+    return a, a.ctypes.data_as(_i32p)
+
+
+class Pager:
+    """The host page allocator (lnk_pager_*): calls marshalled to the C ABI."""
+
+    def __init__(self, num_pages: int, num_rows: int, pages_per_row: int):
+        h = c_vp()
+        _check(_lib.lnk_pager_create(num_pages, num_rows, pages_per_row, ctypes.byref(h)), "lnk_pager_create")
+        self._h = h
+        self.num_pages, self.num_rows, self.pages_per_row = num_pages, num_rows, pages_per_row
+
+    def close(self):
+        if self._h:
+            _lib.lnk_pager_destroy(self._h)
+            self._h = c_vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reserve(self, row: int, length: int):
+        _check(_lib.lnk_pager_reserve(self._h, row, length), "lnk_pager_reserve")
+
+    def fork(self, src_row: int, dst_row: int, length: int):
+        _check(_lib.lnk_pager_fork(self._h, src_row, dst_row, length), "lnk_pager_fork")
+
+    def prepare_append(self, rows, positions):
+        """Returns the (old, new) page copies the append needs, in order."""
+        r, rp = _i32_array(rows)
+        q, qp = _i32_array(positions)
+        n = len(r)
+        src, srcp = _i32_array([0] * max(1, n))
+        dst, dstp = _i32_array([0] * max(1, n))
+        nc = c_i32(0)
+        _check(_lib.lnk_pager_prepare_append(self._h, rp, qp, n, srcp, dstp, ctypes.byref(nc)),
+               "lnk_pager_prepare_append")
+        return [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+
+    def release(self, row: int):
+        _check(_lib.lnk_pager_release(self._h, row), "lnk_pager_release")
+
+    def table(self):
+        import numpy as np
+        t = np.empty((self.num_rows, self.pages_per_row), dtype=np.int32)
+        _check(_lib.lnk_pager_table(self._h, t.ctypes.data_as(_i32p)), "lnk_pager_table")
+        return t
+
+    def free_pages(self) -> int:
+        return int(_lib.lnk_pager_free_pages(self._h))
+
+    def refcount(self, page: int) -> int:
+        return int(_lib.lnk_pager_refcount(self._h, page))
 
 
 def raw_status(fn_name: str, *args) -> int:

@@ -138,6 +138,7 @@ const char* lnk_status_string(lnk_status s) {
     case LNK_ECUDA: return "LNK_ECUDA: CUDA runtime error";
     case LNK_EUNSUPPORTED: return "LNK_EUNSUPPORTED: unsupported shape";
     case LNK_EWORKSPACE: return "LNK_EWORKSPACE: workspace missing or too small";
+    case LNK_ENOSPACE: return "LNK_ENOSPACE: not enough free pages";
   }
   return "unknown lnk_status";
 }
