@@ -108,6 +108,17 @@ def normal_bf16(key: int, start: int, count: int) -> np.ndarray:
     return f32_to_bf16_bits(normal_f32(key, start, count))
 
 
+def e4m3_codes(key: int, start: int, count: int) -> np.ndarray:
+    """Bytes for a prefilled 8-bit (E4M3) pool: from SplitMix64 output i, the
+    sign is bit 63, the exponent field 4 + (bits 8.. mod 6) and the mantissa
+    bits 16..18, so every code is finite with magnitude in [2^-3, 2^3)."""
+    h = splitmix64(key, start, count)
+    sign = (h >> np.uint64(63)) & np.uint64(1)
+    e = np.uint64(4) + ((h >> np.uint64(8)) % np.uint64(6))
+    m = (h >> np.uint64(16)) & np.uint64(7)
+    return ((sign << np.uint64(7)) | (e << np.uint64(3)) | m).astype(np.uint8)
+
+
 def tensor_bf16(seed: int, stream: int, shape) -> np.ndarray:
     n = int(np.prod(shape)) if len(shape) else 1
     return normal_bf16(stream_key(seed, stream), 0, n).reshape(shape)
@@ -209,6 +220,20 @@ class Workload:
         n = self.hkv * self.pool_positions * self.head_dim
         return normal_bf16(self.pool_key(which), 0, n).reshape(
             self.hkv, self.pool_positions, self.head_dim)
+
+    def pool_e4m3(self, which: str) -> np.ndarray:
+        """The whole 8-bit pool [Hkv][num_pages * 64][D] of codes (prefilled context)."""
+        n = self.hkv * self.pool_positions * self.head_dim
+        return e4m3_codes(self.pool_key(which), 0, n).reshape(self.hkv, self.pool_positions, self.head_dim)
+
+    def pool_pages_e4m3(self, which: str, kv_head: int, pages: np.ndarray) -> np.ndarray:
+        """Codes of the listed pages of one kv head, [len(pages)][64][D]."""
+        per_head = self.pool_positions * self.head_dim
+        out = np.empty((len(pages), PAGE_SIZE, self.head_dim), dtype=np.uint8)
+        for i, pg in enumerate(np.asarray(pages).tolist()):
+            start = kv_head * per_head + int(pg) * PAGE_SIZE * self.head_dim
+            out[i] = e4m3_codes(self.pool_key(which), start, PAGE_SIZE * self.head_dim).reshape(PAGE_SIZE, self.head_dim)
+        return out
 
     def pool_pages(self, which: str, kv_head: int, pages: np.ndarray) -> np.ndarray:
         """Initial content of the given physical pages of one kv head: ``[n, 64, D]``."""

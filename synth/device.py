@@ -16,6 +16,9 @@ def _load():
         _lib.synth_fill_normal_bf16.restype = ctypes.c_int
         _lib.synth_fill_normal_bf16.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_ulonglong,
                                                 ctypes.c_longlong, ctypes.c_void_p]
+        _lib.synth_fill_e4m3.restype = ctypes.c_int
+        _lib.synth_fill_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_ulonglong,
+                                         ctypes.c_longlong, ctypes.c_void_p]
     return _lib
 
 
@@ -25,5 +28,15 @@ def fill_normal_bf16(tensor, key: int, start: int = 0, stream=None):
     lib = _load()
     s = torch.cuda.current_stream().cuda_stream if stream is None else stream
     err = lib.synth_fill_normal_bf16(tensor.data_ptr(), tensor.numel(), key, start, s)
+    if err != 0:
+        raise RuntimeError(f"synth fill failed: CUDA error {err}")
+
+
+def fill_e4m3(tensor, key: int, start: int = 0, stream=None):
+    """Fill a contiguous 8-bit device tensor with prefilled-pool codes start.. of stream `key`."""
+    import torch
+    lib = _load()
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    err = lib.synth_fill_e4m3(tensor.data_ptr(), tensor.numel(), key, start, s)
     if err != 0:
         raise RuntimeError(f"synth fill failed: CUDA error {err}")

@@ -29,7 +29,36 @@ __global__ void fill_kernel(uint16_t* out, long long n, unsigned long long key, 
   }
 }
 
+// Bytes of a prefilled 8-bit (E4M3) pool: sign = bit 63, exponent field
+// 4 + (bits 8.. mod 6), mantissa = bits 16..18 of SplitMix64 output i.
+__global__ void fill_e4m3_kernel(uint8_t* out, long long n, unsigned long long key, long long start) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const unsigned long long h = mix64(key + static_cast<unsigned long long>(start + i + 1) * kGamma);
+    const unsigned sign = static_cast<unsigned>(h >> 63);
+    const unsigned e = 4u + static_cast<unsigned>((h >> 8) % 6ull);
+    const unsigned m = static_cast<unsigned>((h >> 16) & 7ull);
+    out[i] = static_cast<uint8_t>((sign << 7) | (e << 3) | m);
+  }
+}
+
+long long grid_for(long long n) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (n + 255) / 256;
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * 16;
+  return blocks > cap ? cap : blocks;
+}
+
 }  // namespace
+
+extern "C" int synth_fill_e4m3(uint8_t* out, long long n, unsigned long long key, long long start, void* stream) {
+  if (n <= 0) return 0;
+  fill_e4m3_kernel<<<static_cast<unsigned>(grid_for(n)), 256, 0, static_cast<cudaStream_t>(stream)>>>(out, n, key,
+                                                                                                   start);
+  return static_cast<int>(cudaGetLastError());
+}
 
 extern "C" int synth_fill_normal_bf16(uint16_t* out, long long n, unsigned long long key, long long start,
                                       void* stream) {
