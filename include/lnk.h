@@ -85,7 +85,29 @@ typedef struct lnk_attn_desc {
   int32_t window;         /* 0: none; else key j is visible to a query at p
                              iff p - window < j <= p (itself and window - 1 before) */
   float scale;            /* softmax scale; 0 selects 1 / sqrt(head_dim) */
+  int32_t kv_dtype;       /* element type of k_pool / v_pool: LNK_KV_BF16 (0, the
+                             pages' pools) or LNK_KV_E4M3 (8-bit pools, below) */
+  float k_scale;          /* LNK_KV_E4M3: a K code c stands for e4m3(c) * k_scale (> 0, finite) */
+  float v_scale;          /* LNK_KV_E4M3: a V code c stands for e4m3(c) * v_scale (> 0, finite) */
 } lnk_attn_desc;
+
+/* Pool element types (lnk_attn_desc.kv_dtype).
+ *
+ * LNK_KV_BF16: bfloat16 pools, as on the pages.
+ * LNK_KV_E4M3: 8-bit pools (not on the pages; an option of this library that
+ *   halves the bytes of the HBM-bound decode path).  Elements are OCP E4M3
+ *   codes (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+ *   subnormals, no infinities, S.1111.111 = NaN, largest finite 448), one
+ *   byte each: the pools are [Hkv][num_pages * 64][D] bytes and the lnk_bf16*
+ *   pool arguments of every entry point point to those bytes.  The append
+ *   stores code = round-to-nearest-even E4M3 of fl32(value / scale), where
+ *   value is the bf16 value a bf16 pool would hold (the rotated K, the V
+ *   input) and the division is one IEEE float32 division, saturating to
+ *   +-448.  Attention uses the dequantized values e4m3(c) * scale.  Chunk
+ *   attention (P > 0 in lnk_paged_step_attn) is supported on bf16 pools only;
+ *   decode rows are supported on both. */
+#define LNK_KV_BF16 0
+#define LNK_KV_E4M3 1
 
 /* Rotary frequencies: inv_freq[i] = exp(-(f32(i) * 2 / f32(D)) * log(theta))
  * in float32 ("Phi-3 Mini 4K Instruct -- files", src/rope.linnet, tables),
@@ -136,7 +158,8 @@ size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows);
  *   table    device int32 [num_rows][pages_per_row] (unused when slots != NULL)
  *   q_norm_w, k_norm_w  device [D] QK-norm weights, or NULL for no QK-norm
  *   norm_eps QK-norm epsilon (1e-6 for Qwen3)
- *   k_pool, v_pool  device pools (written at the tokens' slots only)
+ *   k_pool, v_pool  device pools (written at the tokens' slots only; 8-bit
+ *            codes for LNK_KV_E4M3, see lnk_attn_desc.kv_dtype)
  *   q_out    device [T][Hq][D]   rotated queries (zero for inactive tokens)
  *   T        tokens (0 is allowed and enqueues nothing)
  *
@@ -166,7 +189,7 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  *   q_roped  device [B][Hq][D]  rotated queries (q_out of append_rope), 16-byte aligned
  *   positions device int32 [B]  position of row b's token (< 0: inactive row)
  *   table    device int32 [num_rows][pages_per_row]; decode row b uses table row b
- *   k_pool, v_pool device pools
+ *   k_pool, v_pool device pools (bf16, or 8-bit codes for LNK_KV_E4M3)
  *   out      device [B][Hq][D]  attention output (bf16, nearest even), 8-byte aligned
  *   B        decode rows, 0 <= B <= min(num_rows, 4096)
  *   workspace device scratch of ws_bytes >= lnk_paged_workspace_size(desc, B)
@@ -200,7 +223,8 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
  *   out       device [P + B][Hq][D]
  *   last      device int32 [M] or NULL: chunk token whose output row is copied
  *             to last_out[m] (device [M][Hq][D]); M may be 0
- *   P, B      chunk tokens and decode rows (either may be 0)
+ *   P, B      chunk tokens and decode rows (either may be 0); P > 0 with
+ *             LNK_KV_E4M3 pools returns LNK_EUNSUPPORTED
  *   workspace as for decode_attn with max_rows >= B
  */
 lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
@@ -309,7 +333,8 @@ int32_t lnk_pager_free_pages(const lnk_pager* pager);
 int32_t lnk_pager_refcount(const lnk_pager* pager, int32_t page);
 
 /* Copies pages src_pages[i] -> dst_pages[i] (device int32 arrays of n) in the
- * K and V pools, every kv head (the copy on write of prepare_append).  A pair
+ * K and V pools (of the desc's element type), every kv head (the copy on
+ * write of prepare_append).  A pair
  * with a page outside [0, num_pages) is skipped and sets LNK_DEV_BAD_PAGE in
  * *dev_status.  Pairs must not overlap (no page both a source and a target).
  * Enqueued on `stream`; call it before the append that writes the pages. */

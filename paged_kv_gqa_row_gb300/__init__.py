@@ -6,6 +6,8 @@ and a thin ctypes binding with the C names (``binding.py``).
 """
 from .binding import (  # noqa: F401
     EXPORTED,
+    KV_BF16,
+    KV_E4M3,
     LIBRARY_PATH,
     AttnDesc,
     LnkError,

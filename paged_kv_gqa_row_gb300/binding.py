@@ -41,10 +41,14 @@ class LnkError(RuntimeError):
         super().__init__(f"{where}: {msg}")
 
 
+KV_BF16, KV_E4M3 = 0, 1
+
+
 class AttnDesc(ctypes.Structure):
     _fields_ = [("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
                 ("page_size", c_i32), ("num_pages", c_i32), ("num_rows", c_i32),
-                ("pages_per_row", c_i32), ("window", c_i32), ("scale", c_f32)]
+                ("pages_per_row", c_i32), ("window", c_i32), ("scale", c_f32),
+                ("kv_dtype", c_i32), ("k_scale", c_f32), ("v_scale", c_f32)]
 
 
 class RopeDesc(ctypes.Structure):
@@ -97,9 +101,9 @@ _lib.lnk_paged_copy_pages.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp
 
 
 def attn_desc(num_q_heads, num_kv_heads, head_dim, num_pages, num_rows, pages_per_row,
-              window=0, scale=0.0, page_size=64) -> AttnDesc:
+              window=0, scale=0.0, page_size=64, kv_dtype=KV_BF16, k_scale=1.0, v_scale=1.0) -> AttnDesc:
     return AttnDesc(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, num_rows,
-                    pages_per_row, window, scale)
+                    pages_per_row, window, scale, kv_dtype, k_scale, v_scale)
 
 
 def rope_desc(theta, llama3=None) -> RopeDesc:

@@ -1,5 +1,6 @@
 // C ABI entry points of liblnk: argument checks, frequency tables, tensor
 // maps and launches.  Nothing here allocates device memory or synchronises.
+#include <cfloat>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -38,12 +39,16 @@ EncodeTiledFn encode_fn() {
 bool make_pool_map(CUtensorMap* map, const void* pool, const lnk_attn_desc& d) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+  // 8-bit pools are viewed as 16-bit pairs: a page row of D codes is D / 2
+  // elements, so one 64 x 64 box (128-byte rows) covers a whole page
+  const bool kv8 = d.kv_dtype == LNK_KV_E4M3;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kv8 ? d.head_dim / 2 : d.head_dim),
                         static_cast<cuuint64_t>(d.num_kv_heads) * d.num_pages * kPage};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * (kv8 ? 1 : 2)};
   cuuint32_t box[2] = {kBoxCols, kPage};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+  CUresult r = enc(map, kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(pool), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -61,6 +66,10 @@ lnk_status check_desc(const lnk_attn_desc* d) {
   if (g != 1 && g != 2 && g != 4 && g != 8) return LNK_EUNSUPPORTED;
   if (d->num_pages <= 0 || d->num_rows <= 0 || d->pages_per_row <= 0) return LNK_EINVAL;
   if (d->window < 0 || !(d->scale >= 0.f)) return LNK_EINVAL;
+  if (d->kv_dtype != LNK_KV_BF16 && d->kv_dtype != LNK_KV_E4M3) return LNK_EUNSUPPORTED;
+  if (d->kv_dtype == LNK_KV_E4M3 && !(d->k_scale > 0.f && d->k_scale <= FLT_MAX && d->v_scale > 0.f &&
+                                       d->v_scale <= FLT_MAX))
+    return LNK_EINVAL;
   // TMA row coordinates and 32-bit position arithmetic must not overflow
   if (static_cast<long long>(d->num_kv_heads) * d->num_pages * kPage >= (1ll << 31)) return LNK_ERANGE;
   if (static_cast<long long>(d->pages_per_row) * kPage >= (1ll << 31)) return LNK_ERANGE;
@@ -68,8 +77,11 @@ lnk_status check_desc(const lnk_attn_desc* d) {
   return LNK_OK;
 }
 
+// Softmax scale in log2 units; for 8-bit pools the scores are computed on
+// codes, so the key scale joins it.
 float scale_log2(const lnk_attn_desc* d) {
-  const double s = d->scale > 0.f ? static_cast<double>(d->scale) : 1.0 / std::sqrt(static_cast<double>(d->head_dim));
+  double s = d->scale > 0.f ? static_cast<double>(d->scale) : 1.0 / std::sqrt(static_cast<double>(d->head_dim));
+  if (d->kv_dtype == LNK_KV_E4M3) s *= static_cast<double>(d->k_scale);
   return static_cast<float>(s * 1.4426950408889634);  // log2(e)
 }
 
@@ -197,6 +209,9 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
   p.num_pages = desc->num_pages;
   p.num_rows = desc->num_rows;
   p.pages_per_row = desc->pages_per_row;
+  p.kv8 = desc->kv_dtype == LNK_KV_E4M3;
+  p.k_scale = desc->k_scale;
+  p.v_scale = desc->v_scale;
   return launch_append(p, desc->head_dim, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? LNK_OK
                                                                                                 : LNK_ECUDA;
 }
@@ -207,7 +222,8 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
                                 const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
-  if (decode_prepare(desc->head_dim, B, &launch) != cudaSuccess || launch.grid <= 0) return LNK_ECUDA;
+  const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
+  if (decode_prepare(desc->head_dim, kv8, B, &launch) != cudaSuccess || launch.grid <= 0) return LNK_ECUDA;
   const int group = desc->num_q_heads / desc->num_kv_heads;
   const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
   if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 256)) return LNK_EWORKSPACE;
@@ -229,7 +245,8 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.pages_per_row = desc->pages_per_row;
   p.window = desc->window;
   p.scale_log2 = scale_log2(desc);
-  return launch_decode(kmap, vmap, p, desc->head_dim, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
+  p.out_scale = kv8 ? desc->v_scale : 1.f;
+  return launch_decode(kmap, vmap, p, desc->head_dim, kv8, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
 }
 
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
@@ -264,6 +281,7 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
   if (P > 0 && (!rows || !positions)) return LNK_EINVAL;
   if (B > 0 && !step_positions) return LNK_EINVAL;
   if (M > 0 && (!last || !last_out)) return LNK_EINVAL;
+  if (P > 0 && desc->kv_dtype != LNK_KV_BF16) return LNK_EUNSUPPORTED;  // chunk kernel reads bf16 pools
   if (!aligned(q_roped, 16) || !aligned(out, 8) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
   if (B > 0) {
     const size_t need = lnk_paged_workspace_size(desc, B);

@@ -21,6 +21,8 @@
 // src/attention.linnet (rope + write_tokens in prefill_packed / step_packed);
 // "Qwen3-4B", QK-norm paragraph; "Mistral 7B Instruct v0.3", Entries table
 // (prefill_paged: each token written at its place in the pool).
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace lnk {
@@ -177,6 +179,15 @@ __device__ __forceinline__ uint32_t df_to_bf16(DF v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// E4M3 codes of two bf16 values (low half first) for a pool with `scale`: one
+// IEEE float32 division each, then round to nearest even with saturation to
+// +-448; the low value's code in the low byte.
+__device__ __forceinline__ uint16_t e4m3_pair(uint32_t bits, float scale) {
+  const float2 f = make_float2(__fdiv_rn(__uint_as_float(bits << 16), scale),
+                               __fdiv_rn(__uint_as_float(bits & 0xFFFF0000u), scale));
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendParams p) {
   constexpr int H = D / 2;
@@ -308,12 +319,15 @@ __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendPa
     const int hh = warp + j * kWarps;
     if (hh >= nrot) break;
     const bool is_q = hh < p.hq;
-    uint16_t* dst;
+    uint16_t* dst = nullptr;
+    uint8_t* dst8 = nullptr;  // 8-bit pools: the key row's codes
     if (is_q) {
       dst = p.q_out + (static_cast<size_t>(t) * p.hq + hh) * D;
     } else {
       if (slot < 0) continue;
-      dst = p.k_pool + (hh - p.hq) * pool_head_stride + static_cast<size_t>(slot) * D;
+      const size_t off = (hh - p.hq) * pool_head_stride + static_cast<size_t>(slot) * D;
+      if (p.kv8) dst8 = reinterpret_cast<uint8_t*>(p.k_pool) + off;
+      else dst = p.k_pool + off;
     }
     if (!has) continue;
     if (pos < 0) {  // inactive token: zero query output
@@ -340,15 +354,30 @@ __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendPa
       lo_bits |= df_to_bf16(o1) << (16 * k);
       hi_bits |= df_to_bf16(o2) << (16 * k);
     }
-    *reinterpret_cast<uint32_t*>(dst + e) = lo_bits;
-    *reinterpret_cast<uint32_t*>(dst + H + e) = hi_bits;
+    if (dst8 != nullptr) {
+      *reinterpret_cast<uint16_t*>(dst8 + e) = e4m3_pair(lo_bits, p.k_scale);
+      *reinterpret_cast<uint16_t*>(dst8 + H + e) = e4m3_pair(hi_bits, p.k_scale);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst + e) = lo_bits;
+      *reinterpret_cast<uint32_t*>(dst + H + e) = hi_bits;
+    }
   }
-  // value heads: bit copy into the slot
+  // value heads: bit copy into the slot (8-bit pools: their codes)
   if (slot >= 0) {
     for (int vh = warp; vh < p.hkv; vh += kWarps) {
       const uint4* src = reinterpret_cast<const uint4*>(p.v + (static_cast<size_t>(t) * p.hkv + vh) * D);
-      uint4* dst = reinterpret_cast<uint4*>(p.v_pool + vh * pool_head_stride + static_cast<size_t>(slot) * D);
-      if (lane < D / 8) dst[lane] = src[lane];
+      const size_t off = vh * pool_head_stride + static_cast<size_t>(slot) * D;
+      if (lane < D / 8) {
+        const uint4 x = src[lane];
+        if (p.kv8) {
+          uint2 codes;
+          codes.x = e4m3_pair(x.x, p.v_scale) | (static_cast<uint32_t>(e4m3_pair(x.y, p.v_scale)) << 16);
+          codes.y = e4m3_pair(x.z, p.v_scale) | (static_cast<uint32_t>(e4m3_pair(x.w, p.v_scale)) << 16);
+          reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.v_pool) + off)[lane] = codes;
+        } else {
+          reinterpret_cast<uint4*>(p.v_pool + off)[lane] = x;
+        }
+      }
     }
   }
 }

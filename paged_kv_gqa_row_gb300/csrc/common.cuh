@@ -29,12 +29,14 @@ struct AppendParams {
   const int32_t* table;
   const uint16_t* q_norm_w;
   const uint16_t* k_norm_w;
-  uint16_t* k_pool;
+  uint16_t* k_pool;           // bf16 pools, or the 8-bit code pools when kv8 != 0
   uint16_t* v_pool;
   uint16_t* q_out;
   int32_t* status;
   double norm_eps;
   int T, hq, hkv, num_pages, num_rows, pages_per_row;
+  int kv8;                    // pools hold E4M3 codes
+  float k_scale, v_scale;     // their scales (a code c stands for e4m3(c) * scale)
   float inv_freq[64];
 };
 
@@ -51,7 +53,8 @@ struct DecodeParams {
   float* ws_ml;               // [segments][G][2]: running max (log2 units), sum
   float* ws_o;                // [segments][G][D]: unnormalised partial outputs
   int B, hq, hkv, group, num_pages, pages_per_row, window;
-  float scale_log2;           // softmax scale * log2(e)
+  float scale_log2;           // softmax scale * log2(e) (8-bit pools: times the key scale)
+  float out_scale;            // 1, or the value scale of an 8-bit pool
 };
 
 struct DecodeLaunch {
@@ -65,9 +68,9 @@ struct DecodeWorkspace {
 };
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
-cudaError_t decode_prepare(int head_dim, int B, DecodeLaunch* launch);
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, DecodeLaunch* launch);
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          int head_dim, const DecodeLaunch& launch, cudaStream_t stream);
+                          int head_dim, bool kv8, const DecodeLaunch& launch, cudaStream_t stream);
 
 // ----------------------------------------------------------------- chunk --
 // A chunk-attention CTA holds this many halves of 128 query rows.

@@ -36,6 +36,19 @@
 //    writes the output (whole pairs) or the partial, counter and, for the
 //    last arriver, the merged output of a cut pair.  Consumers never wait on
 //    global memory.
+// 8-bit pools (E4M3 codes, one byte per element): a page of one head is one
+// 128-byte-wide TMA box (the codes viewed as 16-bit pairs), so a stage holds
+// half the bytes and the ring is twice as deep.  The consumers convert codes
+// to f16 (exact) and use the f16 mma.  No byte transposes are needed:
+//  * K: ldmatrix of the 16-bit view gives a lane 4 consecutive dimensions of
+//    one key; read as k = (4c, 4c+1 | 4c+2, 4c+3) of a 16-dimension step,
+//    with the query fragment read in the same order;
+//  * V: a lane loads 4-byte words of keys c, c+4, c+8, c+12 and pairs their
+//    bytes (prmt), so the 16 keys of a step appear in the order
+//    m -> (m & 8) | ((m >> 1) & 3) | ((m & 1) << 2); Q.K takes its key rows
+//    in that same order, so P^T from movmatrix matches; the 4 dimensions a
+//    lane holds make the M rows of two d-tiles, undone when O is staged.
+// The key scale multiplies the softmax scale, the value scale the output.
 // The per-row prologue (visible pages, prefix sums) reads only positions, so
 // it overlaps the previous kernel on the stream (programmatic dependent
 // launch); the kernel waits for that kernel before touching q or the pool.
@@ -57,7 +70,7 @@ constexpr int kThreads = 6 * 32;
 #ifndef LNK_DECODE_STAGES
 #define LNK_DECODE_STAGES 4
 #endif
-constexpr int kStages = LNK_DECODE_STAGES;  // K+V pages in flight per CTA
+constexpr int kStages = LNK_DECODE_STAGES;  // K+V pages in flight per CTA (bf16 pools)
 constexpr int kSegFirst = 1;
 constexpr int kSegLast = 2;
 constexpr int kPairWhole = 4;
@@ -67,9 +80,10 @@ struct StageInfo {
   int b, h, klo, khi, flags, seg, nseg, c0;
 };
 
-template <int D>
+template <int D, bool F8>
 struct DecodeSmem {
-  static constexpr int NB = boxes_for(D);
+  static constexpr int NB = F8 ? 1 : boxes_for(D);         // TMA boxes per page of one head
+  static constexpr int kStages = F8 ? 2 * lnk::kStages : lnk::kStages;
   static constexpr int kStageBytes = 2 * NB * kBoxBytes;  // K boxes, then V boxes
   static constexpr int kQBytes = kMaxGroup * D * 2;       // query rows of the stage's segment
   static constexpr int kOStride = D + 4;                  // padded staging row
@@ -130,12 +144,13 @@ __device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref,
   c.seg = c.b * p.hkv + c.h + static_cast<int>(blockIdx.x);
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-  using L = DecodeSmem<D>;
+  using L = DecodeSmem<D, F8>;
   constexpr int NB = L::NB;
+  constexpr int kStages = L::kStages;
   constexpr int DK = D / 16;  // k-steps of Q.K and d-tiles of P.V
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (whole) {
-          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          const float inv = Ls > 0.f ? p.out_scale / Ls : 0.f;
           uint2 pk;
           pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
           pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc.w += v.w * f;
               }
             }
-            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            const float inv = Ls > 0.f ? p.out_scale / Ls : 0.f;
             uint2 pk;
             pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
             pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
@@ -440,9 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = lane >> 2;   // row within an 8-row group
   const int key0 = warp * 16;
   const uint8_t* stage_base = smem + L::stages;
+  // 8-bit pools: the 16 keys of a step in the order m -> perm(m) (see the top)
+  auto perm = [](int m) { return (m & 8) | ((m >> 1) & 3) | ((m & 1) << 2); };
+  constexpr int NT = F8 ? 8 : DK;  // d-tiles of P.V (8-bit pools: 128 columns, unused ones zero)
 
   uint32_t qf[DK][2];
-  float o[DK][4];
+  float o[NT][4];
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   int nseg_done = 0;
 
@@ -455,16 +473,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool gv = r < G;
 #pragma unroll
       for (int kk = 0; kk < DK; ++kk) {
-        qf[kk][0] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 2 * c) : 0u;
-        qf[kk][1] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 8 + 2 * c) : 0u;
+        if constexpr (F8) {  // dimensions 16kk + 4c .. 4c + 3 as f16 pairs
+          const uint2 w = gv ? *reinterpret_cast<const uint2*>(qs + r * D + kk * 16 + 4 * c) : make_uint2(0u, 0u);
+          qf[kk][0] = bf16x2_to_f16x2(w.x);
+          qf[kk][1] = bf16x2_to_f16x2(w.y);
+        } else {
+          qf[kk][0] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 2 * c) : 0u;
+          qf[kk][1] = gv ? *reinterpret_cast<const uint32_t*>(qs + r * D + kk * 16 + 8 + 2 * c) : 0u;
+        }
       }
 #pragma unroll
-      for (int dt = 0; dt < DK; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+      for (int dt = 0; dt < NT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
       m_a = m_b = -INFINITY;
       l_a = l_b = 0.f;
     }
     const bool work = si.khi > si.klo && si.klo < key0 + 16 && si.khi > key0;
-    uint32_t ka[DK][4], va[DK][4];
+    constexpr int KR = F8 ? (DK + 1) / 2 : DK;  // ldmatrix.x4 of K per step
+    constexpr int VR = F8 ? 4 : DK;             // V fragments per step
+    uint32_t ka[KR][4], va[VR][4];
     if (work) {
       const uint8_t* kbuf = stage_base + size_t(s) * L::kStageBytes;
       const uint8_t* vbuf = kbuf + NB * kBoxBytes;
@@ -485,19 +511,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t kaddr = smem_addr(kbuf);
       const uint32_t vaddr = smem_addr(vbuf);
-      const int kkey = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int vkey = key0 + (lane & 7) + (lane >> 4) * 8;
+      if constexpr (F8) {
+        // K: lane L addresses key perm(m) of matrix row m = ((L >> 3) & 1) * 8 + (L & 7),
+        // 16-byte chunk 2 * jp + (L >> 4)
+        const int kkey = key0 + perm(((lane >> 3) & 1) * 8 + (lane & 7));
 #pragma unroll
-      for (int kk = 0; kk < DK; ++kk) {
-        const int chunk = kk * 2 + (lane >> 4);
-        ldsm_x4(kaddr + (chunk >> 3) * kBoxBytes + swz128(kkey, chunk & 7), ka[kk][0], ka[kk][1], ka[kk][2],
-                ka[kk][3]);
-      }
+        for (int jp = 0; jp < KR; ++jp)
+          ldsm_x4(kaddr + swz128(kkey, 2 * jp + (lane >> 4)), ka[jp][0], ka[jp][1], ka[jp][2], ka[jp][3]);
+        // V: words of keys c + 4i, dimensions 16 * chunk + 4 * (r & 3) .. + 3,
+        // chunk x for r < 4 and x + 4 for r >= 4 (no bank conflicts)
 #pragma unroll
-      for (int dt = 0; dt < DK; ++dt) {
-        const int chunk = dt * 2 + ((lane >> 3) & 1);
-        ldsm_x4_trans(vaddr + (chunk >> 3) * kBoxBytes + swz128(vkey, chunk & 7), va[dt][0], va[dt][1],
-                      va[dt][2], va[dt][3]);
+        for (int x = 0; x < 4; ++x) {
+          const int chunk = x + 4 * (r >> 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            va[x][i] = *reinterpret_cast<const uint32_t*>(vbuf + swz128(key0 + c + 4 * i, chunk) + 4 * (r & 3));
+        }
+      } else {
+        const int kkey = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int vkey = key0 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+        for (int kk = 0; kk < DK; ++kk) {
+          const int chunk = kk * 2 + (lane >> 4);
+          ldsm_x4(kaddr + (chunk >> 3) * kBoxBytes + swz128(kkey, chunk & 7), ka[kk][0], ka[kk][1], ka[kk][2],
+                  ka[kk][3]);
+        }
+#pragma unroll
+        for (int dt = 0; dt < DK; ++dt) {
+          const int chunk = dt * 2 + ((lane >> 3) & 1);
+          ldsm_x4_trans(vaddr + (chunk >> 3) * kBoxBytes + swz128(vkey, chunk & 7), va[dt][0], va[dt][1],
+                        va[dt][2], va[dt][3]);
+        }
       }
     }
     // the fragments are in registers: release the stage before the math
@@ -507,15 +551,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (work) {
       // ---- S^T = K Q^T (two independent accumulation chains) ----
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (F8) {
 #pragma unroll
-      for (int kk = 0; kk < DK; kk += 2) {
-        mma_bf16_16816(sc, ka[kk][0], ka[kk][1], ka[kk][2], ka[kk][3], qf[kk][0], qf[kk][1]);
-        if (kk + 1 < DK)
-          mma_bf16_16816(sd, ka[kk + 1][0], ka[kk + 1][1], ka[kk + 1][2], ka[kk + 1][3], qf[kk + 1][0],
-                         qf[kk + 1][1]);
+        for (int kk = 0; kk < DK; ++kk) {
+          const uint32_t lo = ka[kk >> 1][(kk & 1) * 2], hi = ka[kk >> 1][(kk & 1) * 2 + 1];
+          mma_f16_16816((kk & 1) ? sd : sc, e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(hi), e4m3x2_to_f16x2(lo >> 16),
+                        e4m3x2_to_f16x2(hi >> 16), qf[kk][0], qf[kk][1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < DK; kk += 2) {
+          mma_bf16_16816(sc, ka[kk][0], ka[kk][1], ka[kk][2], ka[kk][3], qf[kk][0], qf[kk][1]);
+          if (kk + 1 < DK)
+            mma_bf16_16816(sd, ka[kk + 1][0], ka[kk + 1][1], ka[kk + 1][2], ka[kk + 1][3], qf[kk + 1][0],
+                           qf[kk + 1][1]);
+        }
       }
       // ---- mask, online softmax (log2 domain) ----
-      const int kr0 = key0 + r, kr1 = kr0 + 8;
+      const int kr0 = key0 + (F8 ? perm(r) : r), kr1 = kr0 + 8;
       const bool v0 = kr0 >= si.klo && kr0 < si.khi;
       const bool v1 = kr1 >= si.klo && kr1 < si.khi;
       const float s0 = v0 ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
@@ -539,15 +592,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_a = mn_a;
       m_b = mn_b;
       // ---- O^T = O^T * alpha + V^T P^T ----
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      if constexpr (F8) {
+        const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
 #pragma unroll
-      for (int dt = 0; dt < DK; ++dt) {
-        o[dt][0] *= al_a;
-        o[dt][1] *= al_b;
-        o[dt][2] *= al_a;
-        o[dt][3] *= al_b;
-        mma_bf16_16816(o[dt], va[dt][0], va[dt][1], va[dt][2], va[dt][3], pb0, pb1);
+        for (int dt = 0; dt < NT; ++dt) {
+          o[dt][0] *= al_a;
+          o[dt][1] *= al_b;
+          o[dt][2] *= al_a;
+          o[dt][3] *= al_b;
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          // bytes (key c, key c+4) and (key c+8, key c+12) of dimensions 0,1 then 2,3
+          const uint32_t e01 = __byte_perm(va[x][0], va[x][1], 0x5140);
+          const uint32_t f01 = __byte_perm(va[x][2], va[x][3], 0x5140);
+          const uint32_t e23 = __byte_perm(va[x][0], va[x][1], 0x7362);
+          const uint32_t f23 = __byte_perm(va[x][2], va[x][3], 0x7362);
+          mma_f16_16816(o[2 * x], e4m3x2_to_f16x2(e01), e4m3x2_to_f16x2(e01 >> 16), e4m3x2_to_f16x2(f01),
+                        e4m3x2_to_f16x2(f01 >> 16), pb0, pb1);
+          mma_f16_16816(o[2 * x + 1], e4m3x2_to_f16x2(e23), e4m3x2_to_f16x2(e23 >> 16), e4m3x2_to_f16x2(f23),
+                        e4m3x2_to_f16x2(f23 >> 16), pb0, pb1);
+        }
+      } else {
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+#pragma unroll
+        for (int dt = 0; dt < DK; ++dt) {
+          o[dt][0] *= al_a;
+          o[dt][1] *= al_b;
+          o[dt][2] *= al_a;
+          o[dt][3] *= al_b;
+          mma_bf16_16816(o[dt], va[dt][0], va[dt][1], va[dt][2], va[dt][3], pb0, pb1);
+        }
       }
     }
 
@@ -569,12 +646,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (warp == 0 && lane == 0) slot_info[slot] = si;
       float* ow = ost + size_t(slot) * L::kSlotFloats + size_t(warp) * kMaxGroup * L::kOStride;
+      if constexpr (F8) {
 #pragma unroll
-      for (int dt = 0; dt < DK; ++dt) {
-        ow[(2 * c) * L::kOStride + dt * 16 + r] = o[dt][0];
-        ow[(2 * c + 1) * L::kOStride + dt * 16 + r] = o[dt][1];
-        ow[(2 * c) * L::kOStride + dt * 16 + r + 8] = o[dt][2];
-        ow[(2 * c + 1) * L::kOStride + dt * 16 + r + 8] = o[dt][3];
+        for (int dt = 0; dt < NT; ++dt) {
+          // d-tile dt: pair x = dt / 2, dimensions 0,1 (even dt) or 2,3 (odd dt) of the lane's word
+          const int d = 16 * (dt / 2 + 4 * (r >> 2)) + 4 * (r & 3) + 2 * (dt & 1);
+          if (d < D) {
+            ow[(2 * c) * L::kOStride + d] = o[dt][0];
+            ow[(2 * c + 1) * L::kOStride + d] = o[dt][1];
+            ow[(2 * c) * L::kOStride + d + 1] = o[dt][2];
+            ow[(2 * c + 1) * L::kOStride + d + 1] = o[dt][3];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int dt = 0; dt < DK; ++dt) {
+          ow[(2 * c) * L::kOStride + dt * 16 + r] = o[dt][0];
+          ow[(2 * c + 1) * L::kOStride + dt * 16 + r] = o[dt][1];
+          ow[(2 * c) * L::kOStride + dt * 16 + r + 8] = o[dt][2];
+          ow[(2 * c + 1) * L::kOStride + dt * 16 + r + 8] = o[dt][3];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(slot_full + slot));
@@ -584,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             const DecodeLaunch& launch, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -597,13 +688,13 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D>, kmap, vmap, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, F8>, kmap, vmap, p);
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t prepare_t(int B, DecodeLaunch* launch) {
-  const size_t bytes = DecodeSmem<D>::bytes(B);
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t bytes = DecodeSmem<D, F8>::bytes(B);
+  cudaError_t err = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   launch->smem_bytes = static_cast<int>(bytes);
@@ -624,22 +715,28 @@ DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_d
   return w;
 }
 
-cudaError_t decode_prepare(int head_dim, int B, DecodeLaunch* launch) {
-  switch (head_dim) {
-    case 64: return prepare_t<64>(B, launch);
-    case 96: return prepare_t<96>(B, launch);
-    case 128: return prepare_t<128>(B, launch);
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, DecodeLaunch* launch) {
+  switch (head_dim * 2 + (kv8 ? 1 : 0)) {
+    case 128: return prepare_t<64, false>(B, launch);
+    case 129: return prepare_t<64, true>(B, launch);
+    case 192: return prepare_t<96, false>(B, launch);
+    case 193: return prepare_t<96, true>(B, launch);
+    case 256: return prepare_t<128, false>(B, launch);
+    case 257: return prepare_t<128, true>(B, launch);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          int head_dim, const DecodeLaunch& launch, cudaStream_t stream) {
+                          int head_dim, bool kv8, const DecodeLaunch& launch, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
-  switch (head_dim) {
-    case 64: return launch_decode_t<64>(kmap, vmap, p, launch, stream);
-    case 96: return launch_decode_t<96>(kmap, vmap, p, launch, stream);
-    case 128: return launch_decode_t<128>(kmap, vmap, p, launch, stream);
+  switch (head_dim * 2 + (kv8 ? 1 : 0)) {
+    case 128: return launch_decode_t<64, false>(kmap, vmap, p, launch, stream);
+    case 129: return launch_decode_t<64, true>(kmap, vmap, p, launch, stream);
+    case 192: return launch_decode_t<96, false>(kmap, vmap, p, launch, stream);
+    case 193: return launch_decode_t<96, true>(kmap, vmap, p, launch, stream);
+    case 256: return launch_decode_t<128, false>(kmap, vmap, p, launch, stream);
+    case 257: return launch_decode_t<128, true>(kmap, vmap, p, launch, stream);
     default: return cudaErrorInvalidValue;
   }
 }
