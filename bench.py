@@ -46,8 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1700.0
 
 
-def algorithmic_bytes(w) -> dict:
-    """Bytes a step must move at least once, by part."""
+def algorithmic_bytes(w, kv_bytes: int = 2) -> dict:
+    """Bytes a step must move at least once, by part (kv_bytes: bytes per pool
+    element, 2 for bf16 pools, 1 for 8-bit pools)."""
     d, hq, hkv = w.head_dim, w.hq, w.hkv
     # decode rows: visible K/V keys, a page shared by several rows counted once
     # (the covered in-page range of a shared page is the union of the rows' ranges)
@@ -69,7 +70,7 @@ def algorithmic_bytes(w) -> dict:
             else:
                 cover[pg] = (aa, zz)
     kv_keys = sum(z - a + 1 for a, z in cover.values())
-    dec_kv = 2 * hkv * kv_keys * d * 2
+    dec_kv = 2 * hkv * kv_keys * d * kv_bytes
     dec_q_out = 2 * w.B * hq * d * 2                     # q read + out written
     dec_table = 4 * table_entries
     # chunk tokens: their rows' visible keys (each key once per row)
@@ -80,9 +81,10 @@ def algorithmic_bytes(w) -> dict:
             lo = max(0, int(p) - w.window + 1) if w.window else 0
             a, z = per_row.get(int(r), (lo, int(p)))
             per_row[int(r)] = (min(a, lo), max(z, int(p)))
-        ch_kv = sum(2 * hkv * (z - a + 1) * d * 2 for a, z in per_row.values())
+        ch_kv = sum(2 * hkv * (z - a + 1) * d * kv_bytes for a, z in per_row.values())
     ch_q_out = 2 * w.P * hq * d * 2
-    append = w.T * (hq + 2 * hkv) * d * 2 + w.T * (hq + 2 * hkv) * d * 2 + 8 * w.T
+    # reads q, k, v; writes q_out and the pool slots
+    append = w.T * (hq + 2 * hkv) * d * 2 + w.T * hq * d * 2 + w.T * 2 * hkv * d * kv_bytes + 8 * w.T
     return {"decode_kv": dec_kv, "decode_q_out": dec_q_out, "decode_table": dec_table,
             "chunk_kv": ch_kv, "chunk_q_out": ch_q_out, "append": append,
             "decode_call": dec_kv + dec_q_out + dec_table,
@@ -208,12 +210,16 @@ def sample_tokens(w, n):
     return sorted(rng.choice(w.P, size=min(w.P, n), replace=False).tolist())
 
 
-def cpu_oracle_sample(w, tokens, repeats=1):
+K_SCALE_E4M3, V_SCALE_E4M3 = 0.25, 0.5  # scales of the 8-bit pools in the e4m3 runs
+
+
+def cpu_oracle_sample(w, tokens, repeats=1, kv="bf16"):
     """Time the oracle (as it stands) on a sample of step tokens: for each, the
     append of the step tokens that write into the pages it reads, then its
     attention; returns (seconds, algorithmic bytes of the sample)."""
     import synth  # noqa: F401
-    from oracle import paged, rope
+    from oracle import fp8, paged, rope
+    e4m3 = kv == "e4m3"
     sample = []
     tp, tr = w.token_positions(), w.token_rows()
     inv = rope.inv_freq(w.theta, w.head_dim, w.llama3)
@@ -225,8 +231,9 @@ def cpu_oracle_sample(w, tokens, repeats=1):
         lps = np.arange(lo // 64, p // 64 + 1)
         pages = w.table[row, lps]
         index = {int(pg): i for i, pg in enumerate(pages)}
-        kp = np.stack([w.pool_pages("k", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
-        vp = np.stack([w.pool_pages("v", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        pool_pages = w.pool_pages_e4m3 if e4m3 else w.pool_pages
+        kp = np.stack([pool_pages("k", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        vp = np.stack([pool_pages("v", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
         writers, slots = [], []
         for u in range(w.T):
             pu = int(tp[u])
@@ -243,11 +250,17 @@ def cpu_oracle_sample(w, tokens, repeats=1):
     nbytes = 0
     for _ in range(repeats):
         for (wi, slots, me, p, kp, vp, ctable, nkeys) in sample:
-            q_out, kp2, vp2 = paged.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None,
-                                                kp, vp, inv, slots=slots, gamma_q=gq,
-                                                gamma_k=gk, eps=w.norm_eps)
-            paged.attention_at(q_out[me], 0, p, ctable, kp2, vp2, w.window)
-            nbytes += 2 * w.hkv * nkeys * w.head_dim * 2 + 2 * w.hq * w.head_dim * 2
+            if e4m3:
+                q_out, kp2, vp2 = fp8.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None, kp, vp,
+                                                  inv, K_SCALE_E4M3, V_SCALE_E4M3, slots=slots, gamma_q=gq,
+                                                  gamma_k=gk, eps=w.norm_eps)
+                fp8.attention_at(q_out[me], 0, p, ctable, kp2, vp2, K_SCALE_E4M3, V_SCALE_E4M3, w.window)
+            else:
+                q_out, kp2, vp2 = paged.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None,
+                                                    kp, vp, inv, slots=slots, gamma_q=gq,
+                                                    gamma_k=gk, eps=w.norm_eps)
+                paged.attention_at(q_out[me], 0, p, ctable, kp2, vp2, w.window)
+            nbytes += 2 * w.hkv * nkeys * w.head_dim * (1 if e4m3 else 2) + 2 * w.hq * w.head_dim * 2
     return time.perf_counter() - t0, nbytes
 
 
@@ -268,10 +281,10 @@ def run_reference(args, rank, world):
     w = synth.build(args.config, scale=args.scale, rows=args.rows)
     rows = sample_tokens(w, args.ref_rows)
     for _ in range(max(0, args.warmup)):
-        cpu_oracle_sample(w, rows[:1])
+        cpu_oracle_sample(w, rows[:1], kv=args.kv)
     secs, nbytes = 0.0, 0
     for _ in range(args.steps):
-        s, nb = cpu_oracle_sample(w, rows)
+        s, nb = cpu_oracle_sample(w, rows, kv=args.kv)
         secs += s
         nbytes += nb
     value = nbytes / secs / 1e9
@@ -281,7 +294,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * secs / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.config, "description": CONFIGS[args.config],
+        "config": {"workload": args.config, "description": CONFIGS[args.config], "kv_dtype": args.kv,
                    "sample_rows_per_step": len(rows)},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{len(rows)} {'decode rows' if w.B else 'chunk tokens'} of the "
@@ -303,8 +316,12 @@ def run_gpu(args, rank, world, dist):
     dev = torch.device("cuda", local)
     seed = None if rank == 0 else 1000 + 97 * rank + synth.WORKLOADS[args.config]
     w = synth.build(args.config, seed=seed, scale=args.scale, rows=args.rows)
-    parts = algorithmic_bytes(w)
-    pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * 2
+    e4m3 = args.kv == "e4m3"
+    if e4m3 and w.P:
+        raise SystemExit("--kv e4m3: chunk attention runs on bf16 pools only; use a decode workload")
+    kv_bytes = 1 if e4m3 else 2
+    parts = algorithmic_bytes(w, kv_bytes)
+    pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * kv_bytes
     copies = args.pool_copies or (2 if pool_bytes < (8 << 30) else 1)
 
     def d16(a):
@@ -316,10 +333,11 @@ def run_gpu(args, rank, world, dist):
     shape = (w.hkv, w.pool_positions, w.head_dim)
     pools = []
     for _ in range(copies):
-        kp = torch.empty(shape, dtype=torch.int16, device=dev)
-        vp = torch.empty(shape, dtype=torch.int16, device=dev)
-        sdev.fill_normal_bf16(kp, w.pool_key("k"))
-        sdev.fill_normal_bf16(vp, w.pool_key("v"))
+        kp = torch.empty(shape, dtype=torch.uint8 if e4m3 else torch.int16, device=dev)
+        vp = torch.empty_like(kp)
+        fill = sdev.fill_e4m3 if e4m3 else sdev.fill_normal_bf16
+        fill(kp, w.pool_key("k"))
+        fill(vp, w.pool_key("v"))
         pools.append((kp, vp))
     q, k, v = d16(w.step_q()), d16(w.step_k()), d16(w.step_v())
     pos, rows, table = d32(w.token_positions()), d32(w.token_rows()), d32(w.table)
@@ -330,7 +348,9 @@ def run_gpu(args, rank, world, dist):
     q_out = torch.zeros_like(q)
     out = torch.zeros_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row, window=w.window)
+    desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row, window=w.window,
+                         kv_dtype=lnk.KV_E4M3 if e4m3 else lnk.KV_BF16, k_scale=K_SCALE_E4M3,
+                         v_scale=V_SCALE_E4M3)
     rd = lnk.rope_desc(w.theta, w.llama3)
     ws_bytes = lnk.lnk_paged_workspace_size(desc, max(1, w.B))
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -467,7 +487,8 @@ def run_gpu(args, rank, world, dist):
                                else "lnk_paged_decode_attn (decode_kernel)"),
                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                    "traffic": recorded_traffic("decode.cu", args.config), "algorithmic_bytes": dec_bytes}
+                    "traffic": recorded_traffic("decode.cu", args.config + ("_e4m3" if e4m3 else "")),
+                    "algorithmic_bytes": dec_bytes}
     else:  # prefill alone: the chunk kernel's contractions, tensor bound
         flops = chunk_flops(w)
         tpeak, tkind = read_tensor_peak()
@@ -483,8 +504,8 @@ def run_gpu(args, rank, world, dist):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.config, "description": CONFIGS[args.config],
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "description": CONFIGS[args.config], "kv_dtype": args.kv,
                    "scale": args.scale, "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.head_dim, "page_size": 64, "num_pages": w.num_pages,
                    "parallelism": f"rows x{world} (independent batches per GPU)",
@@ -504,7 +525,7 @@ def run_gpu(args, rank, world, dist):
         rows_s = sample_tokens(w, args.ref_rows)
         secs, nb, reps = 0.0, 0, 0
         while secs < args.cpu_seconds and reps < 50:
-            s, b = cpu_oracle_sample(w, rows_s)
+            s, b = cpu_oracle_sample(w, rows_s, kv=args.kv)
             secs += s
             nb += b
             reps += 1
@@ -522,6 +543,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="mistral", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="lnk", choices=["lnk", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
+                    help="pool element type (e4m3: 8-bit pools, decode workloads only)")
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

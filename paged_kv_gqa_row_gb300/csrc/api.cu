@@ -161,7 +161,8 @@ lnk_status lnk_rope_inv_freq(const lnk_rope_desc* rope, int32_t head_dim, float*
 
 size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows) {
   if (check_desc(desc) != LNK_OK || max_rows < 0 || max_rows > kMaxDecodeRows) return 0;
-  const int grid = device_sm_count();
+  // the largest grid a call can use: two CTAs per SM for 8-bit pools
+  const int grid = device_sm_count() * (desc->kv_dtype == LNK_KV_E4M3 ? 2 : 1);
   if (grid <= 0) return 0;
   return decode_workspace_layout(max_rows, desc->num_kv_heads, desc->num_q_heads / desc->num_kv_heads,
                                  desc->head_dim, grid)

@@ -38,7 +38,8 @@
 //    global memory.
 // 8-bit pools (E4M3 codes, one byte per element): a page of one head is one
 // 128-byte-wide TMA box (the codes viewed as 16-bit pairs), so a stage holds
-// half the bytes and the ring is twice as deep.  The consumers convert codes
+// half the bytes and two CTAs share an SM (twice the consumer warps for the
+// same bytes in flight).  The consumers convert codes
 // to f16 (exact) and use the f16 mma.  No byte transposes are needed:
 //  * K: ldmatrix of the 16-bit view gives a lane 4 consecutive dimensions of
 //    one key; read as k = (4c, 4c+1 | 4c+2, 4c+3) of a 16-dimension step,
@@ -83,7 +84,7 @@ struct StageInfo {
 template <int D, bool F8>
 struct DecodeSmem {
   static constexpr int NB = F8 ? 1 : boxes_for(D);         // TMA boxes per page of one head
-  static constexpr int kStages = F8 ? 2 * lnk::kStages : lnk::kStages;
+  static constexpr int kStages = lnk::kStages;
   static constexpr int kStageBytes = 2 * NB * kBoxBytes;  // K boxes, then V boxes
   static constexpr int kQBytes = kMaxGroup * D * 2;       // query rows of the stage's segment
   static constexpr int kOStride = D + 4;                  // padded staging row
@@ -145,7 +146,7 @@ __device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref,
 }
 
 template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
   using L = DecodeSmem<D, F8>;
@@ -698,7 +699,13 @@ cudaError_t prepare_t(int B, DecodeLaunch* launch) {
                                          static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   launch->smem_bytes = static_cast<int>(bytes);
-  launch->grid = device_sm_count();
+  int per_sm = 1;
+  if (F8) {  // two CTAs per SM when they fit (shared memory grows with B)
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, F8>, kThreads, bytes);
+    if (err != cudaSuccess) return err;
+    per_sm = per_sm >= 2 ? 2 : 1;
+  }
+  launch->grid = device_sm_count() * per_sm;
   return cudaSuccess;
 }
 
