@@ -382,18 +382,30 @@ __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendPa
   }
 }
 
+template <int D>
+cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
+  // Prefer the largest shared-memory carveout, like the attention kernels that
+  // follow: their CTAs can then start on an SM next to this kernel's (the
+  // attention kernel is launched as a programmatic dependent) without the SM
+  // first switching its L1 / shared-memory split.
+  const cudaError_t attr = cudaFuncSetAttribute(append_rope_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                cudaSharedmemCarveoutMaxShared);
+  if (attr != cudaSuccess) return attr;
+  append_rope_kernel<D><<<p.T, kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
   if (p.hq + p.hkv > kWarps * kMaxHeadsPerWarp) return cudaErrorInvalidValue;
   switch (head_dim) {
-    case 64: append_rope_kernel<64><<<p.T, kWarps * 32, 0, stream>>>(p); break;
-    case 96: append_rope_kernel<96><<<p.T, kWarps * 32, 0, stream>>>(p); break;
-    case 128: append_rope_kernel<128><<<p.T, kWarps * 32, 0, stream>>>(p); break;
+    case 64: return launch_append_t<64>(p, stream);
+    case 96: return launch_append_t<96>(p, stream);
+    case 128: return launch_append_t<128>(p, stream);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace lnk

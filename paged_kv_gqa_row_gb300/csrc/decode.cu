@@ -257,6 +257,9 @@ __global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
     bool stop = false;
     for (int rg = 0; rg < nranges && !stop; ++rg) {
       locate(cur, r_begin[rg], pref, p, start, end, per);
+      // the page of the next step is read one step ahead, so that the table's
+      // latency overlaps the wait for a free stage
+      int next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
       for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
         const int s = k % kStages;
         if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
           break;
         }
         const int lp = cur.first_page + cur.j;
-        const int page = cur.trow[lp];
+        const int page = next_page;
         StageInfo si;
         si.b = cur.b;
         si.h = cur.h;
@@ -301,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
         }
         // advance to the next page-head
         if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per);
+        if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
       }
     }
     // Drain: do not leave the CTA while a copy may still land in its memory.
