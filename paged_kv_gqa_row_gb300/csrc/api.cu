@@ -161,8 +161,8 @@ lnk_status lnk_rope_inv_freq(const lnk_rope_desc* rope, int32_t head_dim, float*
 
 size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows) {
   if (check_desc(desc) != LNK_OK || max_rows < 0 || max_rows > kMaxDecodeRows) return 0;
-  // the largest grid a call can use: two CTAs per SM for 8-bit pools
-  const int grid = device_sm_count() * (desc->kv_dtype == LNK_KV_E4M3 ? 2 : 1);
+  // the largest grid a call can use (two CTAs per SM)
+  const int grid = device_sm_count() * 2;
   if (grid <= 0) return 0;
   return decode_workspace_layout(max_rows, desc->num_kv_heads, desc->num_q_heads / desc->num_kv_heads,
                                  desc->head_dim, grid)
@@ -224,7 +224,8 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
-  if (decode_prepare(desc->head_dim, kv8, B, &launch) != cudaSuccess || launch.grid <= 0) return LNK_ECUDA;
+  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch) != cudaSuccess || launch.grid <= 0)
+    return LNK_ECUDA;
   const int group = desc->num_q_heads / desc->num_kv_heads;
   const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
   if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 256)) return LNK_EWORKSPACE;
@@ -247,7 +248,7 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.window = desc->window;
   p.scale_log2 = scale_log2(desc);
   p.out_scale = kv8 ? desc->v_scale : 1.f;
-  return launch_decode(kmap, vmap, p, desc->head_dim, kv8, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
+  return launch_decode(kmap, vmap, p, desc->head_dim, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
 }
 
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,

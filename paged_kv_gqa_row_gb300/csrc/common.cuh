@@ -60,6 +60,7 @@ struct DecodeParams {
 struct DecodeLaunch {
   int grid;        // persistent CTAs
   int smem_bytes;  // dynamic shared memory per CTA
+  int mode;        // kernel variant (pool type, CTAs per SM)
 };
 
 // Workspace layout for `rows` decode rows and `grid` CTAs (byte offsets).
@@ -68,9 +69,9 @@ struct DecodeWorkspace {
 };
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
-cudaError_t decode_prepare(int head_dim, bool kv8, int B, DecodeLaunch* launch);
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch);
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          int head_dim, bool kv8, const DecodeLaunch& launch, cudaStream_t stream);
+                          int head_dim, const DecodeLaunch& launch, cudaStream_t stream);
 
 // ----------------------------------------------------------------- chunk --
 // A chunk-attention CTA holds this many halves of 128 query rows.

@@ -81,10 +81,16 @@ struct StageInfo {
   int b, h, klo, khi, flags, seg, nseg, c0;
 };
 
-template <int D, bool F8>
+// Kernel variants: bf16 pools with one CTA per SM (4 stages), bf16 pools
+// with two CTAs per SM (2 stages each, for launches with many (row, kv head)
+// pairs), 8-bit pools with two CTAs per SM (4 stages of half the bytes).
+constexpr int kModeBf16 = 0, kModeBf16Two = 1, kModeE4m3 = 2;
+
+template <int D, int MODE>
 struct DecodeSmem {
+  static constexpr bool F8 = MODE == kModeE4m3;
   static constexpr int NB = F8 ? 1 : boxes_for(D);         // TMA boxes per page of one head
-  static constexpr int kStages = lnk::kStages;
+  static constexpr int kStages = MODE == kModeBf16Two ? 2 : lnk::kStages;
   static constexpr int kStageBytes = 2 * NB * kBoxBytes;  // K boxes, then V boxes
   static constexpr int kQBytes = kMaxGroup * D * 2;       // query rows of the stage's segment
   static constexpr int kOStride = D + 4;                  // padded staging row
@@ -145,11 +151,12 @@ __device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref,
   c.seg = c.b * p.hkv + c.h + static_cast<int>(blockIdx.x);
 }
 
-template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-  using L = DecodeSmem<D, F8>;
+  using L = DecodeSmem<D, MODE>;
+  constexpr bool F8 = L::F8;
   constexpr int NB = L::NB;
   constexpr int kStages = L::kStages;
   constexpr int DK = D / 16;  // k-steps of Q.K and d-tiles of P.V
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? 2 : 1)
   if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
 }
 
-template <int D, bool F8>
+template <int D, int MODE>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             const DecodeLaunch& launch, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -693,23 +700,24 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, F8>, kmap, vmap, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, MODE>, kmap, vmap, p);
 }
 
-template <int D, bool F8>
+template <int D, int MODE>
 cudaError_t prepare_t(int B, DecodeLaunch* launch) {
-  const size_t bytes = DecodeSmem<D, F8>::bytes(B);
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t bytes = DecodeSmem<D, MODE>::bytes(B);
+  cudaError_t err = cudaFuncSetAttribute(decode_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   launch->smem_bytes = static_cast<int>(bytes);
   int per_sm = 1;
-  if (F8) {  // two CTAs per SM when they fit (shared memory grows with B)
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, F8>, kThreads, bytes);
+  if (MODE != kModeBf16) {  // two CTAs per SM when they fit (shared memory grows with B)
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, MODE>, kThreads, bytes);
     if (err != cudaSuccess) return err;
     per_sm = per_sm >= 2 ? 2 : 1;
   }
   launch->grid = device_sm_count() * per_sm;
+  launch->mode = MODE;
   return cudaSuccess;
 }
 
@@ -726,28 +734,39 @@ DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_d
   return w;
 }
 
-cudaError_t decode_prepare(int head_dim, bool kv8, int B, DecodeLaunch* launch) {
-  switch (head_dim * 2 + (kv8 ? 1 : 0)) {
-    case 128: return prepare_t<64, false>(B, launch);
-    case 129: return prepare_t<64, true>(B, launch);
-    case 192: return prepare_t<96, false>(B, launch);
-    case 193: return prepare_t<96, true>(B, launch);
-    case 256: return prepare_t<128, false>(B, launch);
-    case 257: return prepare_t<128, true>(B, launch);
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch) {
+  // bf16 pools: two CTAs per SM (twice the warps, finer pieces) when there are
+  // at least two (row, kv head) pairs per CTA of that grid, so that few pairs
+  // are cut between CTAs; fewer pairs keep one CTA per SM and deeper rings.
+  const int mode = kv8 ? kModeE4m3
+                       : (static_cast<long long>(B) * hkv >= 4ll * device_sm_count() ? kModeBf16Two : kModeBf16);
+  switch (head_dim * 4 + mode) {
+    case 256: return prepare_t<64, kModeBf16>(B, launch);
+    case 257: return prepare_t<64, kModeBf16Two>(B, launch);
+    case 258: return prepare_t<64, kModeE4m3>(B, launch);
+    case 384: return prepare_t<96, kModeBf16>(B, launch);
+    case 385: return prepare_t<96, kModeBf16Two>(B, launch);
+    case 386: return prepare_t<96, kModeE4m3>(B, launch);
+    case 512: return prepare_t<128, kModeBf16>(B, launch);
+    case 513: return prepare_t<128, kModeBf16Two>(B, launch);
+    case 514: return prepare_t<128, kModeE4m3>(B, launch);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          int head_dim, bool kv8, const DecodeLaunch& launch, cudaStream_t stream) {
+                          int head_dim, const DecodeLaunch& launch, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
-  switch (head_dim * 2 + (kv8 ? 1 : 0)) {
-    case 128: return launch_decode_t<64, false>(kmap, vmap, p, launch, stream);
-    case 129: return launch_decode_t<64, true>(kmap, vmap, p, launch, stream);
-    case 192: return launch_decode_t<96, false>(kmap, vmap, p, launch, stream);
-    case 193: return launch_decode_t<96, true>(kmap, vmap, p, launch, stream);
-    case 256: return launch_decode_t<128, false>(kmap, vmap, p, launch, stream);
-    case 257: return launch_decode_t<128, true>(kmap, vmap, p, launch, stream);
+  switch (head_dim * 4 + launch.mode) {
+    case 256: return launch_decode_t<64, kModeBf16>(kmap, vmap, p, launch, stream);
+    case 257: return launch_decode_t<64, kModeBf16Two>(kmap, vmap, p, launch, stream);
+    case 258: return launch_decode_t<64, kModeE4m3>(kmap, vmap, p, launch, stream);
+    case 384: return launch_decode_t<96, kModeBf16>(kmap, vmap, p, launch, stream);
+    case 385: return launch_decode_t<96, kModeBf16Two>(kmap, vmap, p, launch, stream);
+    case 386: return launch_decode_t<96, kModeE4m3>(kmap, vmap, p, launch, stream);
+    case 512: return launch_decode_t<128, kModeBf16>(kmap, vmap, p, launch, stream);
+    case 513: return launch_decode_t<128, kModeBf16Two>(kmap, vmap, p, launch, stream);
+    case 514: return launch_decode_t<128, kModeE4m3>(kmap, vmap, p, launch, stream);
     default: return cudaErrorInvalidValue;
   }
 }

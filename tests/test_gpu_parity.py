@@ -80,6 +80,9 @@ DECODE_CASES = [
     ("inactive-rows", 8, 2, 128, [100, 1, 257, 64], 0, (1, 3)),
     ("many-short-rows", 32, 8, 128, [17] * 40 + [65] * 9, 0, ()),
     ("one-row-long", 32, 8, 128, [40000], 0, ()),
+    # enough (row, kv head) pairs for the two-CTAs-per-SM variant (B * Hkv >= 4 * SMs)
+    ("many-pairs", 32, 8, 128, [1 + (37 * i) % 700 for i in range(80)], 0, ()),
+    ("many-pairs-mha96-window", 16, 16, 96, [1 + (53 * i) % 900 for i in range(40)], 300, ()),
 ]
 
 
