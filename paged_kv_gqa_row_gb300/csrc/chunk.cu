@@ -50,6 +50,7 @@ constexpr int kStages = 4;
 constexpr int kRows = 128;                // query rows per half = tensor-memory lanes
 constexpr int kTileRows = kRows * kHalves;
 constexpr float kRescaleLog2 = 8.f;       // rescale O when the max grows by more than 2^8
+constexpr int kMaxOrderedTiles = 512;     // tiles ordered by cost (larger launches keep token order)
 
 struct PageInfo {
   int run, key_base, valid, pad;
@@ -72,9 +73,11 @@ struct TcSmem {
   static constexpr size_t info = bars + kNumBars * sizeof(uint64_t);
   static constexpr size_t tok = info + kStages * sizeof(PageInfo);
   static constexpr size_t runs = tok + 4 * kTileRows * 4;
-  static constexpr size_t misc = runs + 4 * kTileRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base
+  static constexpr size_t misc = runs + 4 * kTileRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base, [4] tile
+  static constexpr size_t cost = misc + 64;                   // [kMaxOrderedTiles] estimated pages per tile
+  static constexpr size_t end = cost + kMaxOrderedTiles * 4;
   // more than half of the shared memory, so that one CTA holds the tensor memory of an SM
-  static constexpr size_t bytes = (misc + 64 + 1024) > 120 * 1024 ? (misc + 64 + 1024) : 120 * 1024;
+  static constexpr size_t bytes = (end + 1024) > 120 * 1024 ? (end + 1024) : 120 * 1024;
 };
 
 template <int D>
@@ -110,8 +113,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int G = p.group;
   const int TQ = kHalves * p.tile_tokens;  // tokens of the tile
-  const int tile = p.num_tiles - 1 - static_cast<int>(blockIdx.x);  // later tokens first
-  const int h = blockIdx.y;
+  // Longest tiles first: CTAs are dispatched in launch order, so the CTA of
+  // launch rank L takes the (L / Hkv)-th tile by estimated cost (pages up to
+  // its last position) and kv head L % Hkv.  Every CTA computes the same order.
+  int tile, h;
+  if (p.num_tiles <= kMaxOrderedTiles) {
+    int* cost = reinterpret_cast<int*>(smem + L::cost);
+    for (int i = tid; i < p.num_tiles; i += kThreads) {
+      const int a = p.positions[i * TQ], b = p.positions[min(p.P, (i + 1) * TQ) - 1];
+      const int pm = max(a, b);
+      cost[i] = pm >= 0 ? pm / kPage + 1 : 0;
+    }
+    __syncthreads();
+    const int rank_wanted = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) / p.hkv;
+    for (int i = tid; i < p.num_tiles; i += kThreads) {
+      const int ci = cost[i];
+      int rank = 0;
+      for (int k = 0; k < p.num_tiles; ++k) {
+        const int ck = cost[k];
+        rank += (ck > ci) || (ck == ci && k > i);  // ties: later tokens first
+      }
+      if (rank == rank_wanted) misc[4] = i;
+    }
+    __syncthreads();
+    tile = misc[4];
+    h = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) % p.hkv;
+  } else {
+    tile = p.num_tiles - 1 - static_cast<int>(blockIdx.x);  // later tokens first
+    h = blockIdx.y;
+  }
   const int t0 = tile * TQ;
   const int nt = min(TQ, p.P - t0);
 
