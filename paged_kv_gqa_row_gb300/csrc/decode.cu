@@ -566,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       if constexpr (F8) {
 #pragma unroll
         for (int kk = 0; kk < DK; ++kk) {
-          const uint32_t lo = ka[kk >> 1][(kk & 1) * 2], hi = ka[kk >> 1][(kk & 1) * 2 + 1];
-          mma_f16_16816((kk & 1) ? sd : sc, e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(hi), e4m3x2_to_f16x2(lo >> 16),
-                        e4m3x2_to_f16x2(hi >> 16), qf[kk][0], qf[kk][1]);
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(ka[kk >> 1][(kk & 1) * 2], a0, a2);
+          e4m3x4_to_f16x2x2(ka[kk >> 1][(kk & 1) * 2 + 1], a1, a3);
+          mma_f16_16816((kk & 1) ? sd : sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         }
       } else {
 #pragma unroll
@@ -621,10 +622,13 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           const uint32_t f01 = __byte_perm(va[x][2], va[x][3], 0x5140);
           const uint32_t e23 = __byte_perm(va[x][0], va[x][1], 0x7362);
           const uint32_t f23 = __byte_perm(va[x][2], va[x][3], 0x7362);
-          mma_f16_16816(o[2 * x], e4m3x2_to_f16x2(e01), e4m3x2_to_f16x2(e01 >> 16), e4m3x2_to_f16x2(f01),
-                        e4m3x2_to_f16x2(f01 >> 16), pb0, pb1);
-          mma_f16_16816(o[2 * x + 1], e4m3x2_to_f16x2(e23), e4m3x2_to_f16x2(e23 >> 16), e4m3x2_to_f16x2(f23),
-                        e4m3x2_to_f16x2(f23 >> 16), pb0, pb1);
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(e01, a0, a1);
+          e4m3x4_to_f16x2x2(f01, a2, a3);
+          mma_f16_16816(o[2 * x], a0, a1, a2, a3, pb0, pb1);
+          e4m3x4_to_f16x2x2(e23, a0, a1);
+          e4m3x4_to_f16x2x2(f23, a2, a3);
+          mma_f16_16816(o[2 * x + 1], a0, a1, a2, a3, pb0, pb1);
         }
       } else {
         const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));

@@ -176,6 +176,16 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// Four E4M3 codes of `w` to two pairs of f16 (bytes 0,1 -> lo, bytes 2,3 ->
+// hi; low byte in the low half), reading the two 16-bit halves of `w`
+// directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // Two E4M3 codes (low byte first) to two f16, low half first (exact: every
 // E4M3 value is an f16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
