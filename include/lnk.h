@@ -193,7 +193,9 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  *   out      device [B][Hq][D]  attention output (bf16, nearest even), 8-byte aligned
  *   B        decode rows, 0 <= B <= min(num_rows, 4096)
  *   workspace device scratch of ws_bytes >= lnk_paged_workspace_size(desc, B)
- *             (256-byte aligned; zero-filled before its first use)
+ *             (256-byte aligned; zero-filled before its first use, and again
+ *             after a call that reported LNK_DEV_TIMEOUT; the kernel leaves
+ *             its counters at zero otherwise)
  */
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
                                  const int32_t* positions, const int32_t* table,

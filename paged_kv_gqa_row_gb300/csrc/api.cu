@@ -236,6 +236,7 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.table = table;
   p.out = out;
   p.status = dev_status;
+  p.ws_next = reinterpret_cast<int32_t*>(ws + w.next);
   p.ws_count = reinterpret_cast<int32_t*>(ws + w.count);
   p.ws_ml = reinterpret_cast<float*>(ws + w.ml);
   p.ws_o = reinterpret_cast<float*>(ws + w.o);

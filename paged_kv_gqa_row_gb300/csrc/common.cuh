@@ -49,6 +49,7 @@ struct DecodeParams {
   const int32_t* table;       // [num_rows][pages_per_row]
   uint16_t* out;              // [B][Hq][D]
   int32_t* status;
+  int32_t* ws_next;           // next chunk to claim (zero at rest)
   int32_t* ws_count;          // [B][Hkv] finished segments of cut pairs (zero at rest)
   float* ws_ml;               // [segments][G][2]: running max (log2 units), sum
   float* ws_o;                // [segments][G][D]: unnormalised partial outputs
@@ -65,8 +66,9 @@ struct DecodeLaunch {
 
 // Workspace layout for `rows` decode rows and `grid` CTAs (byte offsets).
 struct DecodeWorkspace {
-  size_t count, ml, o, total;
+  size_t next, count, ml, o, total;  // the counters (next, count) come first and must start at zero
 };
+constexpr int kChunksPerCta = 4;  // decode work chunks per persistent CTA
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
 cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch);

@@ -4,17 +4,20 @@
 // [max(0, p - window + 1), p], i.e. np_b pages of 64 (the first and last may
 // be partial).  Each (row, kv head) pair is a run of np_b page-heads; the runs
 // of all pairs, (b, h) with h fastest, are laid end to end and the resulting
-// stream of page-heads is cut into gridDim.x equal pieces, one per persistent
-// CTA, so every CTA moves the same number of pages whatever the length mix.
-// The part of a pair inside one CTA is a segment.  A pair that falls inside
-// one CTA is finished there (output written directly).  A pair cut by CTA
-// boundaries leaves one partial result per CTA (unnormalised output, running
-// max, running sum; pair q on CTA c writes segment q + c, unique because
-// consecutive pairs never go back to an earlier CTA); each such CTA then
-// increments the pair's counter, and the last one to arrive merges the
-// partials and writes the output (the counter returns to zero).  A CTA
-// processes the segment it shares with the next CTA first, so that cut pairs
-// finish early instead of in the tail.
+// stream of page-heads is cut into equal chunks: one per persistent CTA, or
+// kChunksPerCta per CTA when the launch has many (row, kv head) pairs (at
+// least 5 per CTA).  CTA c starts with chunk c and then claims further chunks
+// from a counter in the workspace, so that CTAs whose pages arrive slower
+// take fewer chunks (the last claimant returns the counter to zero).  The
+// part of a pair inside one chunk is a segment.  A pair that falls inside one
+// chunk is finished there (output written directly).  A pair cut by chunk
+// boundaries leaves one partial result per chunk (unnormalised output,
+// running max, running sum; pair q in chunk i writes segment q + i, unique
+// because consecutive pairs never go back to an earlier chunk); each such
+// chunk then increments the pair's counter, and the last one to arrive merges
+// the partials and writes the output (the counter returns to zero).  Within a
+// chunk, the segment it shares with the next chunk is processed first, so
+// that cut pairs finish early instead of in the tail.
 //
 // CTA structure (192 threads, warp-specialised):
 //  * warp 4, producer: one lane walks the CTA's page-heads, reads the page
@@ -75,7 +78,7 @@ constexpr int kStages = LNK_DECODE_STAGES;  // K+V pages in flight per CTA (bf16
 constexpr int kSegFirst = 1;
 constexpr int kSegLast = 2;
 constexpr int kPairWhole = 4;
-constexpr int kCtaLast = 8;
+constexpr int kEnd = 8;   // no more work: passed from the producer to the consumers and the epilogue
 
 struct StageInfo {
   int b, h, klo, khi, flags, seg, nseg, c0;
@@ -128,7 +131,7 @@ struct Cursor {
 };
 
 __device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref, const DecodeParams& p,
-                                       long long start, long long end, long long per) {
+                                       long long start, long long end, long long per, long long chunk) {
   int lo_b = 0, hi_b = p.B - 1;  // largest b with hkv * pref[b] <= gi
   while (lo_b < hi_b) {
     const int mid = (lo_b + hi_b + 1) >> 1;
@@ -148,7 +151,7 @@ __device__ __forceinline__ void locate(Cursor& c, long long gi, const int* pref,
   c.whole = pair_start >= start && pair_end <= end;
   c.c0 = static_cast<int>(pair_start / per);
   c.nseg = static_cast<int>((pair_end - 1) / per) - c.c0 + 1;
-  c.seg = c.b * p.hkv + c.h + static_cast<int>(blockIdx.x);
+  c.seg = c.b * p.hkv + c.h + static_cast<int>(chunk);
 }
 
 template <int D, int MODE>
@@ -224,9 +227,13 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   }
 
   const long long total = static_cast<long long>(pref[B]) * p.hkv;
-  const long long per = (total + gridDim.x - 1) / gridDim.x;
-  const long long start = min(total, static_cast<long long>(blockIdx.x) * per);
-  const long long end = min(total, start + per);
+  // Several chunks per CTA only when pairs are many (and so short) against a
+  // CTA's share: each chunk boundary cuts a pair, and a cut pair costs a
+  // partial result and a merge.
+  // (8-bit pools: the consumers, not the memory, set the pace; one chunk.)
+  const int chunks_per_cta = !F8 && static_cast<long long>(B) * p.hkv >= 5ll * gridDim.x ? kChunksPerCta : 1;
+  const long long per = (total + chunks_per_cta * gridDim.x - 1) / (chunks_per_cta * gridDim.x);  // chunk size
+  const long long nchunks = per > 0 ? (total + per - 1) / per : 0;
 
   // Wait for the previous kernel on the stream (it writes q and the pool).
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -238,80 +245,100 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       for (int i = tid; i < p.hq * D / 2; i += kThreads) o[i] = 0u;
     }
   }
-  if (start >= end) return;
-  const int nsteps = static_cast<int>(end - start);
+  if (static_cast<long long>(blockIdx.x) >= nchunks) return;
 
   if (warp == kProducerWarp) {
     // ============================== producer ==============================
     if (lane != 0) return;
-    // Order: the CTA's last segment first when its pair continues into the
-    // next CTA, then everything else in stream order.
-    Cursor cur;
-    locate(cur, end - 1, pref, p, start, end, per);
-    const long long last_seg = max(start, end - 1 - cur.j);
-    const bool last_cut = (end - 1 - cur.j) + cur.np > end;
-    long long r_begin[2], r_end[2];
-    int nranges = 1;
-    if (last_cut && last_seg > start) {
-      r_begin[0] = last_seg; r_end[0] = end;
-      r_begin[1] = start;    r_end[1] = last_seg;
-      nranges = 2;
-    } else {
-      r_begin[0] = start; r_end[0] = end;
-    }
     const uint32_t q_bytes = static_cast<uint32_t>(G * D * 2);
     int k = 0;
     bool stop = false;
-    for (int rg = 0; rg < nranges && !stop; ++rg) {
-      locate(cur, r_begin[rg], pref, p, start, end, per);
-      // the page of the next step is read one step ahead, so that the table's
-      // latency overlaps the wait for a free stage
-      int next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
-      for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
-        const int s = k % kStages;
-        if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
-          stop = true;
-          break;
-        }
-        const int lp = cur.first_page + cur.j;
-        const int page = next_page;
-        StageInfo si;
-        si.b = cur.b;
-        si.h = cur.h;
-        si.klo = max(cur.lo - lp * kPage, 0);
-        si.khi = min(cur.pos - lp * kPage + 1, kPage);
-        const bool first = gi == r_begin[rg] || cur.j == 0;
-        si.flags = (first ? kSegFirst : 0) | ((gi == r_end[rg] - 1 || cur.j == cur.np - 1) ? kSegLast : 0) |
-                   (cur.whole ? kPairWhole : 0) | (k == nsteps - 1 ? kCtaLast : 0);
-        si.seg = cur.seg;
-        si.nseg = cur.nseg;
-        si.c0 = cur.c0;
-        const bool valid = page >= 0 && page < p.num_pages;
-        if (!valid) {
-          if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
-          si.klo = si.khi = 0;
-        }
-        info[s] = si;
-        const uint32_t fb = smem_addr(full_bar + s);
-        const uint32_t tx = (valid ? static_cast<uint32_t>(L::kStageBytes) : 0u) + (first ? q_bytes : 0u);
-        if (tx) mbar_arrive_expect_tx(fb, tx); else mbar_arrive(fb);
-        if (first) {
-          const uint16_t* qsrc = p.q + (static_cast<size_t>(cur.b) * p.hq + static_cast<size_t>(cur.h) * G) * D;
-          bulk_load(smem_addr(smem + L::qbuf + size_t(s) * L::kQBytes), qsrc, q_bytes, fb);
-        }
-        if (valid) {
-          const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
-          const uint32_t vdst = kdst + NB * kBoxBytes;
-          const int y = (cur.h * p.num_pages + page) * kPage;
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
-            tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
+    Cursor cur;
+    for (long long chunk = blockIdx.x; chunk < nchunks && !stop;) {
+      const long long start = chunk * per, end = min(total, start + per);
+      // Order: the chunk's last segment first when its pair continues into the
+      // next chunk, then everything else in stream order.
+      locate(cur, end - 1, pref, p, start, end, per, chunk);
+      const long long last_seg = max(start, end - 1 - cur.j);
+      const bool last_cut = (end - 1 - cur.j) + cur.np > end;
+      long long r_begin[2], r_end[2];
+      int nranges = 1;
+      if (last_cut && last_seg > start) {
+        r_begin[0] = last_seg; r_end[0] = end;
+        r_begin[1] = start;    r_end[1] = last_seg;
+        nranges = 2;
+      } else {
+        r_begin[0] = start; r_end[0] = end;
+      }
+      for (int rg = 0; rg < nranges && !stop; ++rg) {
+        locate(cur, r_begin[rg], pref, p, start, end, per, chunk);
+        // the page of the next step is read one step ahead, so that the table's
+        // latency overlaps the wait for a free stage
+        int next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
+        for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
+          const int s = k % kStages;
+          if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
           }
+          const int lp = cur.first_page + cur.j;
+          const int page = next_page;
+          StageInfo si;
+          si.b = cur.b;
+          si.h = cur.h;
+          si.klo = max(cur.lo - lp * kPage, 0);
+          si.khi = min(cur.pos - lp * kPage + 1, kPage);
+          const bool first = gi == r_begin[rg] || cur.j == 0;
+          si.flags = (first ? kSegFirst : 0) | ((gi == r_end[rg] - 1 || cur.j == cur.np - 1) ? kSegLast : 0) |
+                     (cur.whole ? kPairWhole : 0);
+          si.seg = cur.seg;
+          si.nseg = cur.nseg;
+          si.c0 = cur.c0;
+          const bool valid = page >= 0 && page < p.num_pages;
+          if (!valid) {
+            if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
+            si.klo = si.khi = 0;
+          }
+          info[s] = si;
+          const uint32_t fb = smem_addr(full_bar + s);
+          const uint32_t tx = (valid ? static_cast<uint32_t>(L::kStageBytes) : 0u) + (first ? q_bytes : 0u);
+          if (tx) mbar_arrive_expect_tx(fb, tx); else mbar_arrive(fb);
+          if (first) {
+            const uint16_t* qsrc = p.q + (static_cast<size_t>(cur.b) * p.hq + static_cast<size_t>(cur.h) * G) * D;
+            bulk_load(smem_addr(smem + L::qbuf + size_t(s) * L::kQBytes), qsrc, q_bytes, fb);
+          }
+          if (valid) {
+            const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+            const uint32_t vdst = kdst + NB * kBoxBytes;
+            const int y = (cur.h * p.num_pages + page) * kPage;
+  #pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
+              tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
+            }
+          }
+          // advance to the next page-head
+          if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per, chunk);
+          if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
         }
-        // advance to the next page-head
-        if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per);
-        if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
+      }
+      // the next chunk: claims are handed out in order, nchunks in all; the
+      // last claimant returns the counter to zero for the next launch
+      const int v = atomicAdd(p.ws_next, 1);
+      if (v == static_cast<int>(nchunks) - 1) atomicExch(p.ws_next, 0);
+      chunk = static_cast<long long>(v) + gridDim.x;
+    }
+    // end of the work: one more stage, carrying no data
+    {
+      const int s = k % kStages;
+      if (stop || (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag))) {
+        // aborted: the consumers stop on the abort flag
+      } else {
+        StageInfo si{};
+        si.flags = kEnd;
+        info[s] = si;
+        mbar_arrive(smem_addr(full_bar + s));
+        ++k;
       }
     }
     // Drain: do not leave the CTA while a copy may still land in its memory.
@@ -334,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       const int slot = n & 1;
       if (!mbar_wait(smem_addr(slot_full + slot), (n >> 1) & 1, abort_flag)) break;
       const StageInfo si = slot_info[slot];
+      if (si.flags & kEnd) break;
       const float* os = ost + size_t(slot) * L::kSlotFloats;
       const float* ms = mst + slot * kConsumerWarps * kMaxGroup;
       const float* ls = lst + slot * kConsumerWarps * kMaxGroup;
@@ -456,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           }
         }
       }
-      if (si.flags & kCtaLast) break;
     }
     if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
     return;
@@ -476,10 +503,18 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   int nseg_done = 0;
 
-  for (int k = 0; k < nsteps; ++k) {
+  for (int k = 0;; ++k) {
     const int s = k % kStages;
     if (!mbar_wait(smem_addr(full_bar + s), (k / kStages) & 1, abort_flag)) break;
     const StageInfo si = info[s];
+    if (si.flags & kEnd) {  // pass the end on to the epilogue
+      const int slot = nseg_done & 1;
+      if (!mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag)) break;
+      if (warp == 0 && lane == 0) slot_info[slot] = si;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(slot_full + slot));
+      break;
+    }
     if (si.flags & kSegFirst) {
       const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + L::qbuf + size_t(s) * L::kQBytes);
       const bool gv = r < G;
@@ -730,8 +765,9 @@ cudaError_t prepare_t(int B, DecodeLaunch* launch) {
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   DecodeWorkspace w;
-  const size_t segs = static_cast<size_t>(rows) * hkv + static_cast<size_t>(grid);
-  w.count = 0;
+  const size_t segs = static_cast<size_t>(rows) * hkv + static_cast<size_t>(kChunksPerCta) * grid;
+  w.next = 0;
+  w.count = 256;
   w.ml = up(w.count + static_cast<size_t>(rows) * hkv * 4);
   w.o = up(w.ml + segs * group * 2 * 4);
   w.total = up(w.o + segs * group * static_cast<size_t>(head_dim) * 4);

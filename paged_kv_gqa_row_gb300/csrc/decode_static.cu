@@ -66,8 +66,11 @@ extern "C" lnk_status lnk_paged_decode_attn_static(const lnk_attn_desc* desc, co
   if (need > lnk::kStaticScratchBytes) return LNK_ERANGE;
   void* scratch = nullptr;
   if (lnk::scratch_address(&scratch) != cudaSuccess || scratch == nullptr) return LNK_ECUDA;
-  // the per-pair counters (the first B * Hkv int32 of the workspace) start at zero
-  const size_t counters = static_cast<size_t>(B) * desc->num_kv_heads * sizeof(int32_t);
+  // the counters at the start of the workspace (chunk claims, per-pair
+  // segments) start at zero
+  const size_t counters =
+      lnk::decode_workspace_layout(B, desc->num_kv_heads, desc->num_q_heads / desc->num_kv_heads, desc->head_dim, 0)
+          .ml;
   if (cudaMemsetAsync(scratch, 0, counters, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return LNK_ECUDA;
   return lnk_paged_decode_attn(desc, q_roped, positions, table, k_pool, v_pool, out, B, scratch,
