@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   float* ost = reinterpret_cast<float*>(smem + L::ostage);
   float* mst = reinterpret_cast<float*>(smem + L::mstage);
   float* lst = reinterpret_cast<float*>(smem + L::lstage);
-  int* misc = reinterpret_cast<int*>(smem + L::misc);  // [0] abort, [2..7] warp sums of the scan
+  int* misc = reinterpret_cast<int*>(smem + L::misc);  // [0] abort, [2..7] warp sums of the scan, [8] longest pair
   volatile int* abort_flag = misc;
   int* pref = reinterpret_cast<int*>(smem + L::pref);
 
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       mbar_init(smem_addr(slot_empty + i), 1);
     }
     misc[0] = 0;
+    misc[8] = 0;  // longest pair (pages)
     fence_mbarrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -205,9 +206,11 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   {
     const int chunk = (B + kThreads - 1) / kThreads;
     const int r0 = min(B, tid * chunk), r1 = min(B, r0 + chunk);
-    int bad = 0, run = 0;
+    int bad = 0, run = 0, longest = 0;
     for (int b = r0; b < r1; ++b) {
-      run += visible_pages(p.positions[b], p.window, p.pages_per_row, &bad);
+      const int np = visible_pages(p.positions[b], p.window, p.pages_per_row, &bad);
+      longest = max(longest, np);
+      run += np;
       pref[b + 1] = run;
     }
     if (bad && p.status != nullptr && blockIdx.x == 0) atomicOr(p.status, bad);
@@ -218,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       if (lane >= o) incl += v;
     }
     if (lane == 31) misc[2 + warp] = incl;
-    __syncthreads();
+    __syncthreads();  // (also orders misc[8] = 0 above before the maxima below)
+    if (longest > 0) atomicMax(misc + 8, longest);
     int off = incl - run;
     for (int w = 0; w < warp; ++w) off += misc[2 + w];
     for (int b = r0; b < r1; ++b) pref[b + 1] += off;
@@ -227,13 +231,29 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   }
 
   const long long total = static_cast<long long>(pref[B]) * p.hkv;
+  const long long pairs = static_cast<long long>(B) * p.hkv;
+  // At most one pair per CTA, none longer than twice a CTA's share: each
+  // chunk is one whole pair (no partial results, no merges).
+  const bool pair_chunks = pairs <= gridDim.x && 2 * ((total + gridDim.x - 1) / gridDim.x) >= misc[8];
   // Several chunks per CTA only when pairs are many (and so short) against a
   // CTA's share: each chunk boundary cuts a pair, and a cut pair costs a
   // partial result and a merge.
   // (8-bit pools: the consumers, not the memory, set the pace; one chunk.)
   const int chunks_per_cta = !F8 && static_cast<long long>(B) * p.hkv >= 5ll * gridDim.x ? kChunksPerCta : 1;
   const long long per = (total + chunks_per_cta * gridDim.x - 1) / (chunks_per_cta * gridDim.x);  // chunk size
-  const long long nchunks = per > 0 ? (total + per - 1) / per : 0;
+  const long long nchunks = pair_chunks ? pairs : (per > 0 ? (total + per - 1) / per : 0);
+  // page-head range of a chunk
+  auto chunk_range = [&](long long c, long long& s0, long long& s1) {
+    if (pair_chunks) {
+      const int b = static_cast<int>(c / p.hkv), h = static_cast<int>(c % p.hkv);
+      const int np = pref[b + 1] - pref[b];
+      s0 = static_cast<long long>(pref[b]) * p.hkv + static_cast<long long>(h) * np;
+      s1 = s0 + np;
+    } else {
+      s0 = c * per;
+      s1 = min(total, s0 + per);
+    }
+  };
 
   // Wait for the previous kernel on the stream (it writes q and the pool).
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -255,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     bool stop = false;
     Cursor cur;
     for (long long chunk = blockIdx.x; chunk < nchunks && !stop;) {
-      const long long start = chunk * per, end = min(total, start + per);
+      long long start, end;
+      chunk_range(chunk, start, end);
+      if (start < end) {
       // Order: the chunk's last segment first when its pair continues into the
       // next chunk, then everything else in stream order.
       locate(cur, end - 1, pref, p, start, end, per, chunk);
@@ -321,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per, chunk);
           if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
         }
+      }
       }
       // the next chunk: claims are handed out in order, nchunks in all; the
       // last claimant returns the counter to zero for the next launch
