@@ -80,6 +80,8 @@ DECODE_CASES = [
     ("inactive-rows", 8, 2, 128, [100, 1, 257, 64], 0, (1, 3)),
     ("many-short-rows", 32, 8, 128, [17] * 40 + [65] * 9, 0, ()),
     ("one-row-long", 32, 8, 128, [40000], 0, ()),
+    ("window-1-sees-itself", 8, 2, 64, [1, 2, 64, 65, 300], 1, ()),
+    ("all-inactive", 8, 2, 128, [5, 6, 7], 0, (0, 1, 2)),
     # enough (row, kv head) pairs for the two-CTAs-per-SM variant (B * Hkv >= 4 * SMs)
     ("many-pairs", 32, 8, 128, [1 + (37 * i) % 700 for i in range(80)], 0, ()),
     ("many-pairs-mha96-window", 16, 16, 96, [1 + (53 * i) % 900 for i in range(40)], 300, ()),
@@ -399,3 +401,35 @@ def test_decode_rows_over_contiguous_caches():
         qo, ck_b, cv_b = paged.append_rope(q[[b]], k[[b]], v[[b]], pos[[b]], [0], ident, ck[b], cv[b], inv)
         want = paged.attention_at(qo[0], 0, int(pos[b]), ident, ck_b, cv_b, 0)
         assert_attention_close(got[b], want, f"row {b}")
+
+
+def test_decode_max_rows():
+    """The largest decode batch (4096 rows, ragged short lengths): many pairs,
+    claimed chunks, the workspace at its largest for the shape; one more row
+    is refused."""
+    import paged_kv_gqa_row_gb300 as lnk
+    lengths = [1 + (97 * i) % 200 for i in range(4096)]
+    w = synth.custom(seed=4096, hq=4, hkv=2, head_dim=64, dec_lengths=lengths)
+    _check_full(w)
+    d = lnk.attn_desc(4, 2, 64, w.num_pages, 4097, w.pages_per_row)
+    dev = DeviceStep(w, fill="host")
+    with pytest.raises(lnk.LnkError) as e:
+        lnk.lnk_paged_decode_attn(d, dev.q_out, dev.dec_positions, dev.table, dev.k_pool, dev.v_pool, dev.out,
+                                  4097, dev.workspace, dev.ws_bytes)
+    assert e.value.status == 2  # LNK_ERANGE
+
+
+def test_chunk_many_tiles_keep_token_order():
+    """A prompt long enough for more tiles than the kernel orders by cost
+    (17000 tokens at G = 8: 532 tiles of 32 tokens), checked on sampled tokens."""
+    from harness import oracle_tokens
+    w = synth.custom(seed=17000, hq=16, hkv=2, head_dim=64, dec_lengths=[], chunks=[(0, 17000)])
+    dev = DeviceStep(w, fill="host")
+    dev.step()
+    _sync()
+    assert int(dev.status.item()) == 0
+    out = to_bits(dev.out)
+    toks = [0, 31, 32, 8000, 16999]
+    want = oracle_tokens(w, toks)
+    for t in toks:
+        assert_attention_close(out[t], want[t], f"token {t}")
