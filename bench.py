@@ -366,14 +366,14 @@ def run_gpu(args, rank, world, dist):
             lnk.lnk_paged_step_attn(desc, q_src, ch[0], ch[1], ch[2], dec_pos, tab, kp, vp, out_dst,
                                     None, None, w.P, w.B, 0, ws, ws_bytes, status, s_handle)
 
-    def step(i, inp, ev=None):
+    def step(i, inp, ev=None, out_dst=None):
         qq, kk, vv, pp, tab = inp
         kp, vp = pools[i % copies]
         lnk.lnk_paged_append_rope(desc, rd, qq, kk, vv, pp, rows, None, tab, gq, gk, w.norm_eps, kp, vp,
                                   q_out, w.T, status, s_handle)
         if ev is not None:
             ev[0].record(stream)
-        attend(kp, vp, q_out, out, tab)
+        attend(kp, vp, q_out, out if out_dst is None else out_dst, tab)
         if ev is not None:
             ev[1].record(stream)
 
@@ -424,8 +424,11 @@ def run_gpu(args, rank, world, dist):
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     clocks = sampler.stop() if sampler else None
 
-    # ---- end to end: the step's inputs from pinned host memory (one packed
-    # buffer, one copy), the C ABI calls, and the result copied back ----
+    # ---- end to end: every step's inputs copied from pinned host memory (one
+    # packed buffer, one copy), the C ABI calls, and the result copied back to
+    # pinned host memory.  As a serving loop would, the two copy directions
+    # run on their own streams with double buffers, so that step i + 1's inputs
+    # and step i - 1's result move while the kernels of step i run. ----
     host_parts = [w.step_q().view(np.uint8).ravel(), w.step_k().view(np.uint8).ravel(),
                   w.step_v().view(np.uint8).ravel(), w.token_positions().astype(np.int32).view(np.uint8),
                   np.ascontiguousarray(w.table, dtype=np.int32).view(np.uint8).ravel()]
@@ -433,40 +436,69 @@ def run_gpu(args, rank, world, dist):
     h_in = torch.zeros(int(offs[-1]), dtype=torch.uint8).pin_memory()
     for a, o0 in zip(host_parts, offs[:-1]):
         h_in[int(o0):int(o0) + a.size] = torch.from_numpy(a.copy())
-    d_in = torch.empty_like(h_in, device=dev)
+    d_in = [torch.empty_like(h_in, device=dev) for _ in range(2)]
 
-    def view(i, dtype, shape):
-        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-        return d_in[int(offs[i]):int(offs[i]) + n].view(dtype).view(shape)
-
-    e_inputs = (view(0, torch.int16, q.shape), view(1, torch.int16, k.shape), view(2, torch.int16, v.shape),
+    def views(sl):
+        def view(i, dtype, shape):
+            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+            return d_in[sl][int(offs[i]):int(offs[i]) + n].view(dtype).view(shape)
+        return (view(0, torch.int16, q.shape), view(1, torch.int16, k.shape), view(2, torch.int16, v.shape),
                 view(3, torch.int32, pos.shape), view(4, torch.int32, table.shape))
-    h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+
+    e_inputs = [views(0), views(1)]
+    d_out = [torch.zeros_like(out) for _ in range(2)]
+    h_out = [torch.empty(out.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
     h2d = int(sum(a.size for a in host_parts))
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     e2e_steps = max(1, min(args.steps, 200))
+    up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot copied in
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the slot's step finished (inputs read, output written)
+    ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's output copied back
 
-    def e2e_step(i):
-        d_in.copy_(h_in, non_blocking=True)
-        step(i, e_inputs)
-        h_out.copy_(out, non_blocking=True)
+    # Short steps are bound by the host's calls, not the copies: there the
+    # plain loop (copies and kernels in order on one stream) is faster.
+    pipelined = elapsed_ms / args.steps > 0.05
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            e2e_step(i)
-    stream.synchronize()
+    def e2e_run(n):
+        if not pipelined:
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    d_in[0].copy_(h_in, non_blocking=True)
+                    step(i, e_inputs[0], out_dst=d_out[0])
+                    h_out[0].copy_(d_out[0], non_blocking=True)
+            return
+        for i in range(n):
+            sl = i & 1
+            with torch.cuda.stream(up_stream):
+                if i >= 2:
+                    up_stream.wait_event(ev_done[sl])
+                d_in[sl].copy_(h_in, non_blocking=True)
+                ev_in[sl].record(up_stream)
+            stream.wait_event(ev_in[sl])
+            if i >= 2:
+                stream.wait_event(ev_back[sl])
+            with torch.cuda.stream(stream):
+                step(i, e_inputs[sl], out_dst=d_out[sl])
+                ev_done[sl].record(stream)
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(ev_done[sl])
+                h_out[sl].copy_(d_out[sl], non_blocking=True)
+                ev_back[sl].record(down_stream)
+
+    e2e_run(3)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(e2e_steps):
-            e2e_step(i)
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(up_stream if pipelined else stream)
+    e2e_run(e2e_steps)
+    e1.record(down_stream if pipelined else stream)
+    torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
-    assert np.array_equal(h_out.numpy(), out.cpu().numpy()), "end-to-end result differs from the device result"
+    last = (e2e_steps - 1) & 1 if pipelined else 0
+    assert np.array_equal(h_out[last].numpy(), out.cpu().numpy()), "end-to-end result differs from the device result"
 
     vals = torch.tensor([elapsed_ms, e2e_ms, dec_avg_ms], dtype=torch.float64, device=dev)
     if dist:
@@ -517,7 +549,11 @@ def run_gpu(args, rank, world, dist):
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copies": ("every step: inputs host->device and result device->host (pinned), each direction "
+                           "on its own stream overlapping the kernels of the neighbouring steps (double buffers)"
+                           if pipelined else "every step: inputs host->device, the kernels and the result "
+                           "device->host (pinned), in order on one stream")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
