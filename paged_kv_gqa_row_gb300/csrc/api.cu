@@ -3,7 +3,10 @@
 #include <cfloat>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 
 #include "common.cuh"
 
@@ -54,6 +57,34 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const lnk_attn_desc& d) {
   return r == CUDA_SUCCESS;
 }
 
+// make_pool_map with a small per-thread cache: a serving loop passes the same
+// pools every step, and encoding a tensor map costs microseconds of host time.
+bool pool_map(CUtensorMap* map, const void* pool, const lnk_attn_desc& d) {
+  struct Entry {
+    const void* pool = nullptr;
+    int head_dim = 0, num_kv_heads = 0, num_pages = 0, kv_dtype = 0;
+    CUtensorMap map;
+  };
+  thread_local Entry cache[4];
+  thread_local int next = 0;
+  for (const Entry& e : cache)
+    if (e.pool == pool && e.head_dim == d.head_dim && e.num_kv_heads == d.num_kv_heads &&
+        e.num_pages == d.num_pages && e.kv_dtype == d.kv_dtype) {
+      *map = e.map;
+      return true;
+    }
+  if (!make_pool_map(map, pool, d)) return false;
+  Entry& e = cache[next];
+  next = (next + 1) % 4;
+  e.pool = pool;
+  e.head_dim = d.head_dim;
+  e.num_kv_heads = d.num_kv_heads;
+  e.num_pages = d.num_pages;
+  e.kv_dtype = d.kv_dtype;
+  e.map = *map;
+  return true;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shape checks shared by every entry point.
@@ -86,6 +117,56 @@ float scale_log2(const lnk_attn_desc* d) {
 }
 
 }  // namespace
+
+cudaError_t set_max_dynamic_smem(const void* func, int bytes) {
+  // cudaFuncSetAttribute only when a launch needs more than what was set on this device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[{func, dev}];
+  if (have >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) have = bytes;
+  return err;
+}
+
+cudaError_t prefer_max_shared(const void* func) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (err == cudaSuccess) done.insert({func, dev});
+  return err;
+}
+
+cudaError_t occupancy_blocks(int* blocks, const void* func, int threads, size_t bytes) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t>, int> done;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({func, dev, threads, bytes});
+    if (it != done.end()) {
+      *blocks = it->second;
+      return cudaSuccess;
+    }
+  }
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, func, threads, bytes);
+  if (err == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    done[{func, dev, threads, bytes}] = *blocks;
+  }
+  return err;
+}
 
 int device_sm_count() {
   int dev = 0;
@@ -188,8 +269,32 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
   if (rows == nullptr && slots == nullptr && T > desc->num_rows) return LNK_EINVAL;
   AppendParams p;
   std::memset(&p, 0, sizeof(p));
-  st = inv_freq_table(rope, desc->head_dim, p.inv_freq);
-  if (st != LNK_OK) return st;
+  {
+    // the table is the same step after step: keep the last one per thread
+    struct Cached {
+      bool valid = false;
+      int head_dim = 0;
+      lnk_rope_desc rope;
+      float table[64];
+    };
+    thread_local Cached c;
+    const bool hit = c.valid && c.head_dim == desc->head_dim && rope != nullptr && c.rope.theta == rope->theta &&
+                     c.rope.llama3 == rope->llama3 &&
+                     (!rope->llama3 || (c.rope.factor == rope->factor && c.rope.low_freq_factor == rope->low_freq_factor &&
+                                        c.rope.high_freq_factor == rope->high_freq_factor &&
+                                        c.rope.original_max_position == rope->original_max_position));
+    if (!hit) {
+      st = inv_freq_table(rope, desc->head_dim, c.table);
+      if (st != LNK_OK) {
+        c.valid = false;
+        return st;
+      }
+      c.valid = true;
+      c.head_dim = desc->head_dim;
+      c.rope = *rope;
+    }
+    std::memcpy(p.inv_freq, c.table, sizeof(float) * (desc->head_dim / 2));
+  }
   p.q = q;
   p.k = k;
   p.v = v;
@@ -264,7 +369,7 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
   if (!q_roped || !positions || !table || !k_pool || !v_pool || !out) return LNK_EINVAL;
   if (!aligned(q_roped, 16) || !aligned(out, 8) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
   CUtensorMap kmap, vmap;
-  if (!make_pool_map(&kmap, k_pool, *desc) || !make_pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
+  if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
   return decode_common(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
                        kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -291,7 +396,7 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
     if (workspace == nullptr || need == 0 || ws_bytes < need) return LNK_EWORKSPACE;
   }
   CUtensorMap kmap, vmap;
-  if (!make_pool_map(&kmap, k_pool, *desc) || !make_pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
+  if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int group = desc->num_q_heads / desc->num_kv_heads;
   const size_t row_elems = static_cast<size_t>(desc->num_q_heads) * desc->head_dim;

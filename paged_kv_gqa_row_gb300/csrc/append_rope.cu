@@ -388,8 +388,7 @@ cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
   // follow: their CTAs can then start on an SM next to this kernel's (the
   // attention kernel is launched as a programmatic dependent) without the SM
   // first switching its L1 / shared-memory split.
-  const cudaError_t attr = cudaFuncSetAttribute(append_rope_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                cudaSharedmemCarveoutMaxShared);
+  const cudaError_t attr = prefer_max_shared(reinterpret_cast<const void*>(append_rope_kernel<D>));
   if (attr != cudaSuccess) return attr;
   append_rope_kernel<D><<<p.T, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();

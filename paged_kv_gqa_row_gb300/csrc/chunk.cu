@@ -504,8 +504,7 @@ template <int D>
 cudaError_t launch_chunk_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkParams& p,
                            cudaStream_t stream) {
   const int bytes = static_cast<int>(TcSmem<D>::bytes);
-  cudaError_t err =
-      cudaFuncSetAttribute(chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t err = set_max_dynamic_smem(reinterpret_cast<const void*>(chunk_kernel<D>), bytes);
   if (err != cudaSuccess) return err;
   dim3 grid(p.num_tiles, p.hkv);
   chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(kmap, vmap, p);

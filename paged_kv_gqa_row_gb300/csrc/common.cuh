@@ -102,4 +102,9 @@ cudaError_t launch_gather_last(const uint16_t* out, const int32_t* last, uint16_
 // ------------------------------------------------------------- device info --
 int device_sm_count();
 
+// Host-side launch set-up, done once per device (and size) instead of per call.
+cudaError_t set_max_dynamic_smem(const void* func, int bytes);
+cudaError_t prefer_max_shared(const void* func);
+cudaError_t occupancy_blocks(int* blocks, const void* func, int threads, size_t bytes);
+
 }  // namespace lnk

@@ -768,13 +768,13 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
 template <int D, int MODE>
 cudaError_t prepare_t(int B, DecodeLaunch* launch) {
   const size_t bytes = DecodeSmem<D, MODE>::bytes(B);
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
+  const void* fn = reinterpret_cast<const void*>(decode_kernel<D, MODE>);
+  cudaError_t err = set_max_dynamic_smem(fn, static_cast<int>(bytes));
   if (err != cudaSuccess) return err;
   launch->smem_bytes = static_cast<int>(bytes);
   int per_sm = 1;
   if (MODE != kModeBf16) {  // two CTAs per SM when they fit (shared memory grows with B)
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, MODE>, kThreads, bytes);
+    err = occupancy_blocks(&per_sm, fn, kThreads, bytes);
     if (err != cudaSuccess) return err;
     per_sm = per_sm >= 2 ? 2 : 1;
   }
