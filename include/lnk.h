@@ -344,6 +344,18 @@ lnk_status lnk_paged_copy_pages(const lnk_attn_desc* desc, lnk_bf16* k_pool, lnk
                                 const int32_t* src_pages, const int32_t* dst_pages, int32_t n,
                                 int32_t* dev_status, lnk_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * Self-test of the bounded waits.  Every wait inside the kernels above is
+ * bounded: after about two seconds it gives up, the CTA's other roles stop,
+ * the kernel ORs LNK_DEV_TIMEOUT into *dev_status and returns (no trap, no
+ * fault).  This call runs that path on purpose: one CTA of two warps waits on
+ * pipeline barriers that nothing arrives at; the first gives up after
+ * limit_ns (1 .. 2e9), the second must then stop through the CTA's abort flag
+ * rather than its own two-second limit.  dev_status (device) receives
+ * LNK_DEV_TIMEOUT.  LNK_EINVAL for a null status or a limit out of range.
+ * ------------------------------------------------------------------------- */
+lnk_status lnk_selftest_wait_timeout(int32_t* dev_status, uint64_t limit_ns, lnk_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,6 +5,7 @@ this package holds its CUDA sources (``csrc/``), the build step (``build.py``)
 and a thin ctypes binding with the C names (``binding.py``).
 """
 from .binding import (  # noqa: F401
+    DEV_TIMEOUT,
     EXPORTED,
     KV_BF16,
     KV_E4M3,
@@ -21,6 +22,7 @@ from .binding import (  # noqa: F401
     lnk_paged_step_attn,
     lnk_paged_workspace_size,
     lnk_rope_inv_freq,
+    lnk_selftest_wait_timeout,
     lnk_status_string,
     rope_desc,
 )

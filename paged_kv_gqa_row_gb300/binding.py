@@ -31,7 +31,8 @@ EXPORTED = ["lnk_status_string", "lnk_rope_inv_freq", "lnk_paged_workspace_size"
             "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_step_attn",
             "lnk_paged_decode_attn_static", "lnk_pager_create", "lnk_pager_destroy", "lnk_pager_reserve",
             "lnk_pager_fork", "lnk_pager_prepare_append", "lnk_pager_release", "lnk_pager_table",
-            "lnk_pager_free_pages", "lnk_pager_refcount", "lnk_paged_copy_pages"]
+            "lnk_pager_free_pages", "lnk_pager_refcount", "lnk_paged_copy_pages",
+            "lnk_selftest_wait_timeout"]
 
 
 class LnkError(RuntimeError):
@@ -98,6 +99,8 @@ _lib.lnk_pager_refcount.restype = c_i32
 _lib.lnk_pager_refcount.argtypes = [c_vp, c_i32]
 _lib.lnk_paged_copy_pages.restype = ctypes.c_int
 _lib.lnk_paged_copy_pages.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp]
+_lib.lnk_selftest_wait_timeout.restype = ctypes.c_int
+_lib.lnk_selftest_wait_timeout.argtypes = [c_vp, ctypes.c_uint64, c_vp]
 
 
 def attn_desc(num_q_heads, num_kv_heads, head_dim, num_pages, num_rows, pages_per_row,
@@ -189,6 +192,11 @@ def lnk_paged_copy_pages(desc, k_pool, v_pool, src_pages, dst_pages, n, dev_stat
     st = _lib.lnk_paged_copy_pages(ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(src_pages),
                                    _ptr(dst_pages), n, _ptr(dev_status), _stream(stream))
     _check(st, "lnk_paged_copy_pages")
+
+
+def lnk_selftest_wait_timeout(dev_status, limit_ns, stream=None):
+    st = _lib.lnk_selftest_wait_timeout(_ptr(dev_status), int(limit_ns), _stream(stream))
+    _check(st, "lnk_selftest_wait_timeout")
 
 
 def _i32_array(values):

@@ -271,13 +271,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && npages > 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(kRows, 64, 0, 0);
       constexpr uint32_t kIdPV = umma_idesc_bf16(kRows, L::kPvN, 0, 1);
+      // Descriptors of stage 0's K (K-major) and V (MN-major) boxes; another
+      // stage or K step adds its byte offset / 16 to the 14-bit address field,
+      // which cannot carry (shared addresses stay below 256 KiB).
+      const uint32_t stage0 = smem_addr(smem + L::stages);
+      const uint64_t kdesc0 = umma_desc_sw128(stage0, 0, 1024);
+      const uint64_t vdesc0 = umma_desc_sw128(stage0 + NB * kBoxBytes, kBoxBytes, 1024);
       // S_hf = Q_hf K^T for the page in stage s (Q from tensor memory)
       auto issue_s = [&](int hf, int s) {
-        const uint32_t kaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
         const uint32_t hc = tmem + hf * L::kHalfCols;
 #pragma unroll
         for (int kk = 0; kk < DK; ++kk) {
-          const uint64_t bd = umma_desc_sw128(kaddr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 0, 1024);
+          const uint64_t bd = kd + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
           umma_ts(hc + L::kColS, hc + L::kColQ + kk * 8, bd, kIdS, kk > 0);
         }
         umma_commit(smem_addr(s_full + hf));
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_pv = -1;
       for (int j = 0; ok && j < npages; ++j) {
         const int s = j % kStages;
-        const uint32_t vaddr = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes) + NB * kBoxBytes;
+        const uint64_t vd = vdesc0 + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
 #pragma unroll
         for (int hf = 0; hf < kHalves && ok; ++hf) {
           ok = mbar_wait(smem_addr(p_full + hf), j & 1, abort_flag);
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t hc = tmem + hf * L::kHalfCols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // 64 keys, 16 per instruction
-            const uint64_t bd = umma_desc_sw128(vaddr + kk * 16 * 128, kBoxBytes, 1024);
+            const uint64_t bd = vd + ((kk * 16 * 128) >> 4);
             umma_ts(hc + L::kColO, hc + L::kColS + kk * 8, bd, kIdPV, (j > 0 || kk > 0));
           }
           umma_commit(smem_addr(pv_done + hf));
@@ -358,12 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(q_full));
     }
+    // Every wait's outcome is made warp-uniform: the tensor-memory loads and
+    // stores that follow are warp-collective.
     float m_ref = -INFINITY, l_sum = 0.f;
     uint32_t zero_uses = 0;
     bool ok = true;
     for (int j = 0; j < npages && ok; ++j) {
       const int s = j % kStages;
-      ok = mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag));
       if (!ok) break;
       const PageInfo si = info[s];
       const int kmin = run_kmin[si.run], kmax = run_kmax[si.run];
@@ -379,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(zero_bar));
-        ok = mbar_wait(smem_addr(zero_bar), zero_uses & 1u, abort_flag);
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(zero_bar), zero_uses & 1u, abort_flag));
         ++zero_uses;
       }
       if (!ok) break;
-      ok = mbar_wait(smem_addr(s_full + hf), j & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(s_full + hf), j & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float x[64];
@@ -429,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__any_sync(0xffffffffu, alpha != 1.f) && j >= 1) {
-        ok = mbar_wait(smem_addr(pv_done + hf), (j - 1) & 1, abort_flag);  // P.V of page j - 1
+        // P.V of page j - 1
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(pv_done + hf), (j - 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
@@ -465,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- normalise and store this row ----
     if (ok && npages > 0) {
-      ok = mbar_wait(smem_addr(pv_done + hf), (npages - 1) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(pv_done + hf), (npages - 1) & 1, abort_flag));
       tc_fence_after();
     }
     uint16_t* dst = p.out + qrow;

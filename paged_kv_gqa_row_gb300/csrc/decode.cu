@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     constexpr int D4 = D / 4;
     for (int n = 0;; ++n) {
       const int slot = n & 1;
-      if (!mbar_wait(smem_addr(slot_full + slot), (n >> 1) & 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(slot_full + slot), (n >> 1) & 1, abort_flag))) break;
       const StageInfo si = slot_info[slot];
       if (si.flags & kEnd) break;
       const float* os = ost + size_t(slot) * L::kSlotFloats;
@@ -528,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
 
   for (int k = 0;; ++k) {
     const int s = k % kStages;
-    if (!mbar_wait(smem_addr(full_bar + s), (k / kStages) & 1, abort_flag)) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(full_bar + s), (k / kStages) & 1, abort_flag))) break;
     const StageInfo si = info[s];
     if (si.flags & kEnd) {  // pass the end on to the epilogue
       const int slot = nseg_done & 1;
-      if (!mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag))) break;
       if (warp == 0 && lane == 0) slot_info[slot] = si;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(slot_full + slot));
@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
         lb += __shfl_xor_sync(0xffffffffu, lb, off);
       }
       const int slot = nseg_done & 1;
-      if (!mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(slot_empty + slot), ((nseg_done >> 1) & 1) ^ 1, abort_flag))) break;
       if (lane < 4) {
         mst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c] = m_a;
         mst[(slot * kConsumerWarps + warp) * kMaxGroup + 2 * c + 1] = m_b;

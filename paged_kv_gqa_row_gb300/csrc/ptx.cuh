@@ -65,21 +65,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of the barrier to complete.  Gives up (returns
-// false) when *abort becomes non-zero or after about two seconds, in which
-// case it sets *abort so that the other roles of the CTA stop too.  The
-// iteration count is capped as well, so the loop ends even if the timer
-// does not advance.
+// false) when *abort becomes non-zero or after `limit_ns` (about two seconds
+// unless a self-test asks for less), in which case it sets *abort so that
+// the other roles of the CTA stop too.  The iteration count is capped as
+// well, so the loop ends even if the timer does not advance.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kWaitLimitIters = 1u << 30;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      if (global_timer_ns() - t0 > limit_ns) break;
     }
   }
   *abort = 1;

@@ -41,3 +41,14 @@ def test_binding_lists_every_declared_symbol():
     _ensure_built()
     import paged_kv_gqa_row_gb300 as lnk
     assert sorted(lnk.EXPORTED) == _declared()
+
+
+def test_wait_selftest_refuses_bad_arguments_without_launching():
+    _ensure_built()
+    lib = ctypes.CDLL(LIB)
+    lib.lnk_selftest_wait_timeout.restype = ctypes.c_int
+    lib.lnk_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+    einval = 1
+    assert lib.lnk_selftest_wait_timeout(None, 1000, None) == einval           # no status buffer
+    assert lib.lnk_selftest_wait_timeout(ctypes.c_void_p(16), 0, None) == einval  # no limit
+    assert lib.lnk_selftest_wait_timeout(ctypes.c_void_p(16), 3_000_000_000, None) == einval  # over 2 s
