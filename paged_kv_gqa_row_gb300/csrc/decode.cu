@@ -653,11 +653,13 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
       }
       const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      // no running max of the warp moved: O needs no rescaling (alpha = 1)
+      const bool same_max = __all_sync(0xffffffffu, mn_a == m_a && mn_b == m_b);
       const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
       const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-      const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-      const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
-      const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+      const float al_a = ex2_approx(m_a - base_a), al_b = ex2_approx(m_b - base_b);
+      const float p0 = ex2_approx(s0 - base_a), p1 = ex2_approx(s1 - base_b);
+      const float p2 = ex2_approx(s2 - base_a), p3 = ex2_approx(s3 - base_b);
       l_a = l_a * al_a + (p0 + p2);
       l_b = l_b * al_b + (p1 + p3);
       m_a = mn_a;
@@ -666,12 +668,14 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       if constexpr (F8) {
         const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+        if (!same_max) {
 #pragma unroll
-        for (int dt = 0; dt < NT; ++dt) {
-          o[dt][0] *= al_a;
-          o[dt][1] *= al_b;
-          o[dt][2] *= al_a;
-          o[dt][3] *= al_b;
+          for (int dt = 0; dt < NT; ++dt) {
+            o[dt][0] *= al_a;
+            o[dt][1] *= al_b;
+            o[dt][2] *= al_a;
+            o[dt][3] *= al_b;
+          }
         }
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
@@ -691,14 +695,18 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       } else {
         const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+        if (!same_max) {
 #pragma unroll
-        for (int dt = 0; dt < DK; ++dt) {
-          o[dt][0] *= al_a;
-          o[dt][1] *= al_b;
-          o[dt][2] *= al_a;
-          o[dt][3] *= al_b;
-          mma_bf16_16816(o[dt], va[dt][0], va[dt][1], va[dt][2], va[dt][3], pb0, pb1);
+          for (int dt = 0; dt < DK; ++dt) {
+            o[dt][0] *= al_a;
+            o[dt][1] *= al_b;
+            o[dt][2] *= al_a;
+            o[dt][3] *= al_b;
+          }
         }
+#pragma unroll
+        for (int dt = 0; dt < DK; ++dt)
+          mma_bf16_16816(o[dt], va[dt][0], va[dt][1], va[dt][2], va[dt][3], pb0, pb1);
       }
     }
 
