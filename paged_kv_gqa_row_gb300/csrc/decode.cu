@@ -521,6 +521,20 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   auto perm = [](int m) { return (m & 8) | ((m >> 1) & 3) | ((m & 1) << 2); };
   constexpr int NT = F8 ? 8 : DK;  // d-tiles of P.V (8-bit pools: 128 columns, unused ones zero)
 
+  // 8-bit pools: this lane's shared-memory offsets inside a stage's K and V
+  // boxes (see the loads below), fixed for the whole kernel.  Key rows c + 4i
+  // repeat their swizzle every two steps of i, 1024 bytes apart.
+  uint32_t koff[F8 ? (DK + 1) / 2 : 1], voff[F8 ? 2 : 1][F8 ? 4 : 1];
+  if constexpr (F8) {
+    const int kkey = key0 + perm(((lane >> 3) & 1) * 8 + (lane & 7));
+#pragma unroll
+    for (int jp = 0; jp < (DK + 1) / 2; ++jp) koff[jp] = swz128(kkey, 2 * jp + (lane >> 4));
+#pragma unroll
+    for (int par = 0; par < 2; ++par)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) voff[par][x] = swz128(key0 + c + 4 * par, x + 4 * (r >> 2)) + 4 * (r & 3);
+  }
+
   uint32_t qf[DK][2];
   float o[NT][4];
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
@@ -584,19 +598,15 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       if constexpr (F8) {
         // K: lane L addresses key perm(m) of matrix row m = ((L >> 3) & 1) * 8 + (L & 7),
         // 16-byte chunk 2 * jp + (L >> 4)
-        const int kkey = key0 + perm(((lane >> 3) & 1) * 8 + (lane & 7));
 #pragma unroll
-        for (int jp = 0; jp < KR; ++jp)
-          ldsm_x4(kaddr + swz128(kkey, 2 * jp + (lane >> 4)), ka[jp][0], ka[jp][1], ka[jp][2], ka[jp][3]);
+        for (int jp = 0; jp < KR; ++jp) ldsm_x4(kaddr + koff[jp], ka[jp][0], ka[jp][1], ka[jp][2], ka[jp][3]);
         // V: words of keys c + 4i, dimensions 16 * chunk + 4 * (r & 3) .. + 3,
         // chunk x for r < 4 and x + 4 for r >= 4 (no bank conflicts)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int chunk = x + 4 * (r >> 2);
+        for (int x = 0; x < 4; ++x)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            va[x][i] = *reinterpret_cast<const uint32_t*>(vbuf + swz128(key0 + c + 4 * i, chunk) + 4 * (r & 3));
-        }
+            va[x][i] = *reinterpret_cast<const uint32_t*>(vbuf + voff[i & 1][x] + 1024 * (i >> 1));
       } else {
         const int kkey = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int vkey = key0 + (lane & 7) + (lane >> 4) * 8;
