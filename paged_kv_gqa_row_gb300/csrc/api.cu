@@ -322,10 +322,11 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
                                                                                                 : LNK_ECUDA;
 }
 
+// The pools reach the kernel through their tensor maps (kmap, vmap).
 static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, const int32_t* positions,
-                                const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
-                                lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                                const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+                                const int32_t* table, lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                cudaStream_t stream) {
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
@@ -370,8 +371,8 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
   if (!aligned(q_roped, 16) || !aligned(out, 8) || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return LNK_EINVAL;
   CUtensorMap kmap, vmap;
   if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
-  return decode_common(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
-                       kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  return decode_common(desc, q_roped, positions, table, out, B, workspace, ws_bytes, dev_status, kmap, vmap,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* rows,
@@ -423,7 +424,7 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
     if (launch_chunk(kmap, vmap, c, desc->head_dim, s) != cudaSuccess) return LNK_ECUDA;
   }
   if (B > 0) {
-    st = decode_common(desc, q_roped + static_cast<size_t>(P) * row_elems, step_positions, table, k_pool, v_pool,
+    st = decode_common(desc, q_roped + static_cast<size_t>(P) * row_elems, step_positions, table,
                        out + static_cast<size_t>(P) * row_elems, B, workspace, ws_bytes, dev_status, kmap, vmap, s);
     if (st != LNK_OK) return st;
   }
