@@ -28,8 +28,12 @@
 namespace lnk {
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kMaxHeadsPerWarp = 8;  // rotated heads (Hq + Hkv) <= 128
+constexpr int kMaxRotated = 128;  // rotated heads (Hq + Hkv) per token
+// Warps per token: 16 for small launches (a short per-token chain), WIDE_WARPS
+// when the launch has many tokens per SM (more tokens resident at once).
+constexpr int kWarpsSmall = 16;
+constexpr int kWarpsWide = 8;
+constexpr int kWideTokensPerSm = 4;  // launches with at least this many tokens per SM use kWarpsWide
 
 struct DF {
   float hi, lo;
@@ -188,8 +192,9 @@ __device__ __forceinline__ uint16_t e4m3_pair(uint32_t bits, float scale) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3));
 }
 
-template <int D>
+template <int D, int kWarps>
 __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendParams p) {
+  constexpr int kMaxHeadsPerWarp = kMaxRotated / kWarps;
   constexpr int H = D / 2;
   constexpr int kLanes = D / 4;  // lanes holding data: two elements of each half
   // coefficient sets: [0] queries, [1] keys; [.][0] g_i c_i, [1] g_{i+H} s_i,
@@ -382,23 +387,30 @@ __global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(const AppendPa
   }
 }
 
-template <int D>
-cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
+template <int D, int kWarps>
+cudaError_t launch_append_w(const AppendParams& p, cudaStream_t stream) {
   // Prefer the largest shared-memory carveout, like the attention kernels that
   // follow: their CTAs can then start on an SM next to this kernel's (the
   // attention kernel is launched as a programmatic dependent) without the SM
   // first switching its L1 / shared-memory split.
-  const cudaError_t attr = prefer_max_shared(reinterpret_cast<const void*>(append_rope_kernel<D>));
+  const cudaError_t attr = prefer_max_shared(reinterpret_cast<const void*>(append_rope_kernel<D, kWarps>));
   if (attr != cudaSuccess) return attr;
-  append_rope_kernel<D><<<p.T, kWarps * 32, 0, stream>>>(p);
+  append_rope_kernel<D, kWarps><<<p.T, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
+  if (static_cast<long long>(p.T) >= static_cast<long long>(kWideTokensPerSm) * device_sm_count())
+    return launch_append_w<D, kWarpsWide>(p, stream);
+  return launch_append_w<D, kWarpsSmall>(p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  if (p.hq + p.hkv > kWarps * kMaxHeadsPerWarp) return cudaErrorInvalidValue;
+  if (p.hq + p.hkv > kMaxRotated) return cudaErrorInvalidValue;
   switch (head_dim) {
     case 64: return launch_append_t<64>(p, stream);
     case 96: return launch_append_t<96>(p, stream);
