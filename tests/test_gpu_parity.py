@@ -173,6 +173,17 @@ def test_append_rope_matches_oracle(case):
     _check_full(w)
 
 
+@pytest.mark.parametrize("hq,hkv,d,qkn", [(32, 8, 128, True), (32, 32, 96, False)], ids=["qknorm-128", "mha-96"])
+def test_append_wide_launch_matches_oracle(hq, hkv, d, qkn):
+    # at least 4 tokens per SM: the append takes its 8-warps-per-token form
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 4 * sms + 50
+    w = synth.custom(seed=17, hq=hq, hkv=hkv, head_dim=d, dec_lengths=[300, 9000, 1], theta=1e6, qk_norm=qkn,
+                     chunks=[(0, n // 2), (1000, n - n // 2)])
+    assert w.T >= 4 * sms
+    _check_full(w)
+
+
 def test_append_explicit_slots_and_inactive():
     w = synth.custom(seed=12, hq=8, hkv=2, head_dim=128, dec_lengths=[100, 10, 300])
     dev = DeviceStep(w, fill="host")
