@@ -164,9 +164,10 @@ size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows);
  *   T        tokens (0 is allowed and enqueues nothing)
  *
  * Numerics: QK-norm, cos/sin of the float32 angle and the rotation are
- * evaluated in double precision and rounded once to bf16 (nearest even);
- * v is copied bit for bit.  Two tokens writing one slot race (the engine's
- * padding tokens write a shared dump slot nobody reads).
+ * evaluated to about 2^-46 relative (float pairs; double precision for
+ * angles of 2^20 and more and for the QK-norm factor) and rounded once to
+ * bf16 (nearest even); v is copied bit for bit.  Two tokens writing one slot
+ * race (the engine's padding tokens write a shared dump slot nobody reads).
  */
 lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope,
                                  const lnk_bf16* q, const lnk_bf16* k, const lnk_bf16* v,
