@@ -519,12 +519,15 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   const uint8_t* stage_base = smem + L::stages;
   // 8-bit pools: the 16 keys of a step in the order m -> perm(m) (see the top)
   auto perm = [](int m) { return (m & 8) | ((m >> 1) & 3) | ((m & 1) << 2); };
-  constexpr int NT = F8 ? 8 : DK;  // d-tiles of P.V (8-bit pools: 128 columns, unused ones zero)
+  // 8-bit pools: a lane's V words cover 16-dimension chunk x (r < 4) or x + NX
+  // (r >= 4) for x < NX = D / 32, i.e. exactly the D dimensions; d-tiles of P.V
+  constexpr int NX = F8 ? D / 32 : 1;
+  constexpr int NT = F8 ? 2 * NX : DK;
 
   // 8-bit pools: this lane's shared-memory offsets inside a stage's K and V
   // boxes (see the loads below), fixed for the whole kernel.  Key rows c + 4i
   // repeat their swizzle every two steps of i, 1024 bytes apart.
-  uint32_t koff[F8 ? (DK + 1) / 2 : 1], voff[F8 ? 2 : 1][F8 ? 4 : 1];
+  uint32_t koff[F8 ? (DK + 1) / 2 : 1], voff[F8 ? 2 : 1][NX];
   if constexpr (F8) {
     const int kkey = key0 + perm(((lane >> 3) & 1) * 8 + (lane & 7));
 #pragma unroll
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
 #pragma unroll
     for (int par = 0; par < 2; ++par)
 #pragma unroll
-      for (int x = 0; x < 4; ++x) voff[par][x] = swz128(key0 + c + 4 * par, x + 4 * (r >> 2)) + 4 * (r & 3);
+      for (int x = 0; x < NX; ++x) voff[par][x] = swz128(key0 + c + 4 * par, x + NX * (r >> 2)) + 4 * (r & 3);
   }
 
   uint32_t qf[DK][2];
@@ -573,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     }
     const bool work = si.khi > si.klo && si.klo < key0 + 16 && si.khi > key0;
     constexpr int KR = F8 ? (DK + 1) / 2 : DK;  // ldmatrix.x4 of K per step
-    constexpr int VR = F8 ? 4 : DK;             // V fragments per step
+    constexpr int VR = F8 ? NX : DK;            // V fragments per step
     uint32_t ka[KR][4], va[VR][4];
     if (work) {
       const uint8_t* kbuf = stage_base + size_t(s) * L::kStageBytes;
@@ -601,9 +604,10 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
 #pragma unroll
         for (int jp = 0; jp < KR; ++jp) ldsm_x4(kaddr + koff[jp], ka[jp][0], ka[jp][1], ka[jp][2], ka[jp][3]);
         // V: words of keys c + 4i, dimensions 16 * chunk + 4 * (r & 3) .. + 3,
-        // chunk x for r < 4 and x + 4 for r >= 4 (no bank conflicts)
+        // chunk x for r < 4 and x + NX for r >= 4 (no bank conflicts when the two
+        // chunks lie in different halves of the 128-byte swizzle, as for D = 128)
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int x = 0; x < NX; ++x)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             va[x][i] = *reinterpret_cast<const uint32_t*>(vbuf + voff[i & 1][x] + 1024 * (i >> 1));
@@ -688,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           }
         }
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
+        for (int x = 0; x < NX; ++x) {
           // bytes (key c, key c+4) and (key c+8, key c+12) of dimensions 0,1 then 2,3
           const uint32_t e01 = __byte_perm(va[x][0], va[x][1], 0x5140);
           const uint32_t f01 = __byte_perm(va[x][2], va[x][3], 0x5140);
@@ -742,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
 #pragma unroll
         for (int dt = 0; dt < NT; ++dt) {
           // d-tile dt: pair x = dt / 2, dimensions 0,1 (even dt) or 2,3 (odd dt) of the lane's word
-          const int d = 16 * (dt / 2 + 4 * (r >> 2)) + 4 * (r & 3) + 2 * (dt & 1);
+          const int d = 16 * (dt / 2 + NX * (r >> 2)) + 4 * (r & 3) + 2 * (dt & 1);
           if (d < D) {
             ow[(2 * c) * L::kOStride + d] = o[dt][0];
             ow[(2 * c + 1) * L::kOStride + d] = o[dt][1];
