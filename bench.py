@@ -131,7 +131,8 @@ def recorded_traffic(kernel_file: str, config: str):
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "paged_kv_gqa_row_gb300", "csrc", kernel_file), "rb").read()
+        with open(os.path.join(ROOT, "paged_kv_gqa_row_gb300", "csrc", kernel_file), "rb") as f:
+            src = f.read()
         entry = rec.get(config)
         if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
             return float(entry["dram_bytes_per_launch"])

@@ -10,7 +10,8 @@ LIB = os.path.join(ROOT, "paged_kv_gqa_row_gb300", "liblnk.so")
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "lnk.h")).read()
+    with open(os.path.join(ROOT, "include", "lnk.h")) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(lnk_[a-z0-9_]+)\s*\(", text)))
 
