@@ -200,6 +200,45 @@ def pin_qknorm_per_head():
     assert np.allclose(y, y1 * gamma, rtol=1e-14, atol=0)
 
 
+def pin_qknorm_before_rope():
+    """The append normalises each head (QK-norm, gamma included) before it rotates
+    ("Qwen3-4B", model description: the norm follows the head split and precedes
+    the rotation).  A rotation keeps the norm of every (i, i + D/2) pair, so with
+    the norm first the pair norms of a token's rotated q and k are the same at
+    every position as at position 0, where the rotation is the identity.  With a
+    gamma of 2 on the first half and 0.5 on the second, rotating first would mix
+    the two halves before gamma weighs them, and the pair norms would change with
+    the position."""
+    rng = np.random.default_rng(14)
+    d, h = 16, 8
+    x_q = _rand_bits(rng, (1, 2, d))
+    x_k = _rand_bits(rng, (1, 1, d))
+    gamma = bf16.from_f64(np.concatenate([np.full(h, 2.0), np.full(h, 0.5)]))
+    positions = np.array([0, 1, 3, 100, 4097, 70001])
+    T = len(positions)
+    q = np.repeat(x_q, T, axis=0)
+    k = np.repeat(x_k, T, axis=0)
+    v = _rand_bits(rng, (T, 1, d))
+    pool = np.zeros((1, 64, d), dtype=np.uint16)
+    inv = rope.inv_freq_plain(10000.0, d)
+    q_out, kp, _ = paged.append_rope(q, k, v, positions, np.zeros(T, dtype=np.int64), None, pool, pool,
+                                     inv, slots=np.arange(T), gamma_q=gamma, gamma_k=gamma, eps=1e-6)
+
+    def pair_norms(bits):
+        y = bf16.to_f64(bits)
+        return np.sqrt(y[..., :h] ** 2 + y[..., h:] ** 2)
+
+    for got in (pair_norms(q_out), pair_norms(kp[0, :T][:, None, :])):
+        # each side is rounded to bf16 once (relative 2^-9 per element)
+        assert np.allclose(got[1:], got[:1], rtol=2.0 ** -7, atol=0), got
+    # the gamma above does separate the orders: rotating first changes the norms
+    ang = rope.angles(1, inv)
+    g = bf16.to_f64(gamma)
+    xq = bf16.to_f64(x_q[0, 0])
+    wrong = rope.qk_norm(rope.rotate(xq, ang), g, 1e-6)
+    assert not np.allclose(pair_norms(bf16.from_f64(wrong)), pair_norms(q_out[0, 0]), rtol=2.0 ** -5, atol=0)
+
+
 # ---------------------------------------------------------------- attention ----
 
 def _identity_pool(values_k, values_v):
@@ -439,9 +478,6 @@ def pin_cache_size():
     assert per_pos * g["max_seq"] == g["gib"] * 2 ** 30
     assert per_pos * g["max_seq_long"] == g["gib_long"] * 2 ** 30
     assert paged.PAGE_SIZE == GOLDEN["page_size"]["page_size"]
-
-
-ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
 def pin_decode_rows_is_identity_table():

@@ -69,6 +69,31 @@ def _slot_offset_wrong(table, row, position):
     return int(table[row, position // 64]) * 64 + (position // 64) % 64
 
 
+def _append_rotate_then_norm(q, k, v, positions, rows, table, k_pool, v_pool, inv,
+                             slots=None, gamma_q=None, gamma_k=None, eps=1e-6):
+    """The append with its two steps swapped: RoPE first, QK-norm second."""
+    from oracle import bf16
+    q_out = np.zeros_like(q, dtype=np.uint16)
+    k_pool = np.array(k_pool, dtype=np.uint16, copy=True)
+    v_pool = np.array(v_pool, dtype=np.uint16, copy=True)
+    for t in range(q.shape[0]):
+        p = int(positions[t])
+        if p < 0:
+            continue
+        ang = rope.angles(p, inv)
+        qf = rope.rotate(bf16.to_f64(q[t]), ang)
+        kf = rope.rotate(bf16.to_f64(k[t]), ang)
+        if gamma_q is not None:
+            qf = rope.qk_norm(qf, bf16.to_f64(gamma_q), eps)
+        if gamma_k is not None:
+            kf = rope.qk_norm(kf, bf16.to_f64(gamma_k), eps)
+        q_out[t] = bf16.from_f64(qf)
+        s = int(slots[t]) if slots is not None else paged.slot_of(table, int(rows[t]), p)
+        k_pool[:, s, :] = bf16.from_f64(kf)
+        v_pool[:, s, :] = v[t]
+    return q_out, k_pool, v_pool
+
+
 MUTATIONS = [
     # (description, module, attribute, replacement, pin that must fail)
     ("query head reads kv head h % Hkv", paged, "kv_head_of",
@@ -91,6 +116,8 @@ MUTATIONS = [
      _qknorm_across_heads, pins.pin_qknorm_per_head),
     ("qk-norm eps outside the square root", rope, "qk_norm",
      _qknorm_eps_outside, pins.pin_qknorm_rms),
+    ("rope before qk-norm", paged, "append_rope",
+     _append_rotate_then_norm, pins.pin_qknorm_before_rope),
     ("llama3 blend weights swapped", rope, "llama3_scale_one",
      _llama3_swapped, pins.pin_llama3_continuity),
     ("frequency exponent missing the factor 2", rope, "inv_freq_plain",
