@@ -1,14 +1,21 @@
 """Benchmark of the paged decode / step attention path on one or more GPUs.
 
-Default workload: one Mistral-7B-v0.3-shaped layer decode step (64 rows,
-32 q / 8 kv heads, head_dim 128, context lengths uniform in [512, 8192],
-pages of 64 shuffled in a pool sized to the total, bf16 synthetic data).
-A step is one pass of the whole path: append_rope over the step's tokens,
-then decode_attn (or step_attn for the Llama step workload).
+Default workload: one Llama-3.1-8B-shaped step_paged layer, the largest
+single-GPU configuration: 128 decode rows of context lengths uniform in
+[1024, 131072] plus 4 packed prompt chunks of 512 tokens at offsets uniform in
+[0, 16384], 32 q / 8 kv heads, head_dim 128, llama3 RoPE, pages of 64 shuffled
+in a ~36 GB pool, bf16 synthetic data.  A step is one pass of the whole path:
+append_rope over the step's tokens, then step_attn (chunks and decode rows), or
+decode_attn for the decode-only workloads.
 
 Metric: achieved HBM GB/s = algorithmic bytes of a step (the visible K/V
 bytes, each page counted once, plus q in, q/k/v append traffic, outputs and
-page-table entries) / step time; row-steps/s alongside.
+page-table entries) / step time; row-steps/s alongside.  The roofline object
+covers the decode kernel (HBM); for steps with prompt chunks it also carries
+the chunk kernel's tensor-core figure (TFLOP/s against the sustained bf16
+peak).  With the default workload the same line also reports the
+Mistral-7B-shaped decode step (64 rows, lengths U[512, 8192]), run in the same
+process, under "mistral".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lnk|reference]
 
@@ -211,30 +218,33 @@ def sample_tokens(w, n):
     return sorted(rng.choice(w.P, size=min(w.P, n), replace=False).tolist())
 
 
+def sample_units(w, n_tokens):
+    """(token, kv head) units of the oracle samples: every kv head of a seeded
+    sample of step tokens."""
+    return [(t, h) for t in sample_tokens(w, n_tokens) for h in range(w.hkv)]
+
+
 K_SCALE_E4M3, V_SCALE_E4M3 = 0.25, 0.5  # scales of the 8-bit pools in the e4m3 runs
 
 
-def cpu_oracle_sample(w, tokens, repeats=1, kv="bf16"):
-    """Time the oracle (as it stands) on a sample of step tokens: for each, the
-    append of the step tokens that write into the pages it reads, then its
-    attention; returns (seconds, algorithmic bytes of the sample)."""
-    import synth  # noqa: F401
-    from oracle import fp8, paged, rope
+def prepare_oracle_sample(w, units, kv="bf16"):
+    """Inputs of the oracle for each (token, kv head) unit: the pages the token
+    reads of that kv head, and the step tokens that write into them (their q
+    heads of the kv head's group, their k and v of the kv head)."""
     e4m3 = kv == "e4m3"
-    sample = []
     tp, tr = w.token_positions(), w.token_rows()
-    inv = rope.inv_freq(w.theta, w.head_dim, w.llama3)
     q_all, k_all, v_all = w.step_q(), w.step_k(), w.step_v()
-    gq, gk = w.gamma_q(), w.gamma_k()
-    for t in tokens:
+    g = w.hq // w.hkv
+    pool_pages = w.pool_pages_e4m3 if e4m3 else w.pool_pages
+    prepared = []
+    for t, h in units:
         p, row = int(tp[t]), int(tr[t])
         lo = max(0, p - w.window + 1) if w.window else 0
         lps = np.arange(lo // 64, p // 64 + 1)
         pages = w.table[row, lps]
         index = {int(pg): i for i, pg in enumerate(pages)}
-        pool_pages = w.pool_pages_e4m3 if e4m3 else w.pool_pages
-        kp = np.stack([pool_pages("k", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
-        vp = np.stack([pool_pages("v", h, pages).reshape(-1, w.head_dim) for h in range(w.hkv)])
+        kp = pool_pages("k", h, pages).reshape(1, -1, w.head_dim)
+        vp = pool_pages("v", h, pages).reshape(1, -1, w.head_dim)
         writers, slots = [], []
         for u in range(w.T):
             pu = int(tp[u])
@@ -244,347 +254,482 @@ def cpu_oracle_sample(w, tokens, repeats=1, kv="bf16"):
             if pg in index:
                 writers.append(u)
                 slots.append(index[pg] * 64 + pu % 64)
+        wi = np.array(writers)
         ctable = np.full((1, lps[-1] + 1), -1, dtype=np.int32)
         ctable[0, lps] = np.arange(len(lps), dtype=np.int32)
-        sample.append((np.array(writers), np.array(slots), writers.index(t), p, kp, vp, ctable, p - lo + 1))
-    t0 = time.perf_counter()
+        prepared.append(dict(q=q_all[wi][:, h * g:(h + 1) * g], k=k_all[wi][:, h:h + 1], v=v_all[wi][:, h:h + 1],
+                             pos=tp[wi], rows=tr[wi], slots=np.array(slots), me=writers.index(t), p=p,
+                             kp=kp, vp=vp, ctable=ctable, nkeys=p - lo + 1))
+    return prepared
+
+
+def run_oracle_sample(w, prepared, kv="bf16"):
+    """Run the oracle (as it stands) on prepared units: for each, the append of
+    the step tokens that write into the pages it reads, then its attention.
+    Returns (wall seconds, CPU seconds of the process, algorithmic bytes)."""
+    from oracle import fp8, paged, rope
+    e4m3 = kv == "e4m3"
+    inv = rope.inv_freq(w.theta, w.head_dim, w.llama3)
+    gq, gk = w.gamma_q(), w.gamma_k()
+    g = w.hq // w.hkv
+    c0, t0 = time.process_time(), time.perf_counter()
     nbytes = 0
-    for _ in range(repeats):
-        for (wi, slots, me, p, kp, vp, ctable, nkeys) in sample:
-            if e4m3:
-                q_out, kp2, vp2 = fp8.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None, kp, vp,
-                                                  inv, K_SCALE_E4M3, V_SCALE_E4M3, slots=slots, gamma_q=gq,
-                                                  gamma_k=gk, eps=w.norm_eps)
-                fp8.attention_at(q_out[me], 0, p, ctable, kp2, vp2, K_SCALE_E4M3, V_SCALE_E4M3, w.window)
-            else:
-                q_out, kp2, vp2 = paged.append_rope(q_all[wi], k_all[wi], v_all[wi], tp[wi], tr[wi], None,
-                                                    kp, vp, inv, slots=slots, gamma_q=gq,
-                                                    gamma_k=gk, eps=w.norm_eps)
-                paged.attention_at(q_out[me], 0, p, ctable, kp2, vp2, w.window)
-            nbytes += 2 * w.hkv * nkeys * w.head_dim * (1 if e4m3 else 2) + 2 * w.hq * w.head_dim * 2
-    return time.perf_counter() - t0, nbytes
-
-
-def threads_used():
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        return max([i.get("num_threads", 1) for i in info] + [1])
-    except Exception:
-        return os.cpu_count() or 1
+    for u in prepared:
+        if e4m3:
+            q_out, kp2, vp2 = fp8.append_rope(u["q"], u["k"], u["v"], u["pos"], u["rows"], None, u["kp"], u["vp"],
+                                              inv, K_SCALE_E4M3, V_SCALE_E4M3, slots=u["slots"], gamma_q=gq,
+                                              gamma_k=gk, eps=w.norm_eps)
+            fp8.attention_at(q_out[u["me"]], 0, u["p"], u["ctable"], kp2, vp2, K_SCALE_E4M3, V_SCALE_E4M3,
+                             w.window)
+        else:
+            q_out, kp2, vp2 = paged.append_rope(u["q"], u["k"], u["v"], u["pos"], u["rows"], None, u["kp"], u["vp"],
+                                                inv, slots=u["slots"], gamma_q=gq, gamma_k=gk, eps=w.norm_eps)
+            paged.attention_at(q_out[u["me"]], 0, u["p"], u["ctable"], kp2, vp2, w.window)
+        nbytes += 2 * u["nkeys"] * w.head_dim * (1 if e4m3 else 2) + 2 * g * w.head_dim * 2
+    return time.perf_counter() - t0, time.process_time() - c0, nbytes
 
 
 def run_reference(args, rank, world):
-    """The oracle timed on the host cores, each step a bounded sample of rows."""
+    """The oracle timed on the host cores: exactly `steps` timed steps, each a
+    bounded sample of the workload's (token, kv head) units, sized so that the
+    whole run takes about --ref-seconds."""
     import synth
     if rank != 0:
         return None
     w = synth.build(args.config, scale=args.scale, rows=args.rows)
-    rows = sample_tokens(w, args.ref_rows)
-    for _ in range(max(0, args.warmup)):
-        cpu_oracle_sample(w, rows[:1], kv=args.kv)
-    secs, nbytes = 0.0, 0
+    units = sample_units(w, args.ref_rows)
+    prepared = prepare_oracle_sample(w, units, kv=args.kv)
+    # warm-up: one unit per step; it also gives the time of one unit
+    wsecs = []
+    for i in range(max(0, args.warmup)):
+        s, _, _ = run_oracle_sample(w, prepared[i % len(prepared):i % len(prepared) + 1], kv=args.kv)
+        wsecs.append(s)
+    per_unit = max(1e-4, statistics.median(wsecs)) if wsecs else 0.05
+    n = int(max(1, min(len(prepared), args.ref_seconds / max(1, args.steps) / per_unit)))
+    secs = cpu = 0.0
+    nbytes = 0
+    at = 0
     for _ in range(args.steps):
-        s, nb = cpu_oracle_sample(w, rows, kv=args.kv)
+        chunk = [prepared[(at + i) % len(prepared)] for i in range(n)]
+        at = (at + n) % len(prepared)
+        s, c, nb = run_oracle_sample(w, chunk, kv=args.kv)
         secs += s
+        cpu += c
         nbytes += nb
     value = nbytes / secs / 1e9
-    cores = threads_used()
+    cores = round(cpu / secs, 2)
+    what = "decode rows" if w.B else "chunk tokens"
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * secs / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIGS[args.config], "kv_dtype": args.kv,
-                   "sample_rows_per_step": len(rows)},
+                   "sample_units_per_step": n},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{len(rows)} {'decode rows' if w.B else 'chunk tokens'} of the "
-                                   f"{args.config} workload per step"},
+                         "sample": f"{n} (token, kv head) units per step, cycling through all kv heads of "
+                                   f"{len(prepared) // w.hkv} seeded {what} of the {args.config} workload; "
+                                   f"cores = process CPU time / wall time"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
 
 
+class GpuWorkload:
+    """Device buffers of one workload and the library calls of its step."""
+
+    def __init__(self, args, w, dev, kv):
+        import torch
+
+        import paged_kv_gqa_row_gb300 as lnk
+        from synth import device as sdev
+        self.torch, self.lnk, self.w, self.dev = torch, lnk, w, dev
+        e4m3 = kv == "e4m3"
+        if e4m3 and w.P:
+            raise SystemExit("--kv e4m3: chunk attention runs on bf16 pools only; use a decode workload")
+        self.e4m3 = e4m3
+        self.kv_bytes = 1 if e4m3 else 2
+        self.parts = algorithmic_bytes(w, self.kv_bytes)
+        self.pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * self.kv_bytes
+        self.copies = args.pool_copies or (2 if self.pool_bytes < (8 << 30) else 1)
+
+        def d16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+        def d32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        shape = (w.hkv, w.pool_positions, w.head_dim)
+        self.pools = []
+        for _ in range(self.copies):
+            kp = torch.empty(shape, dtype=torch.uint8 if e4m3 else torch.int16, device=dev)
+            vp = torch.empty_like(kp)
+            fill = sdev.fill_e4m3 if e4m3 else sdev.fill_normal_bf16
+            fill(kp, w.pool_key("k"))
+            fill(vp, w.pool_key("v"))
+            self.pools.append((kp, vp))
+        self.q, self.k, self.v = d16(w.step_q()), d16(w.step_k()), d16(w.step_v())
+        self.pos, self.rows, self.table = d32(w.token_positions()), d32(w.token_rows()), d32(w.table)
+        self.dec_pos = d32(w.dec_positions)
+        self.ch = (d32(w.ch_rows), d32(w.ch_positions), d32(w.ch_segments)) if w.P else (None, None, None)
+        self.gq = None if w.gamma_q() is None else d16(w.gamma_q())
+        self.gk = None if w.gamma_k() is None else d16(w.gamma_k())
+        self.q_out = torch.zeros_like(self.q)
+        self.out = torch.zeros_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row,
+                                  window=w.window, kv_dtype=lnk.KV_E4M3 if e4m3 else lnk.KV_BF16,
+                                  k_scale=K_SCALE_E4M3, v_scale=V_SCALE_E4M3)
+        self.rd = lnk.rope_desc(w.theta, w.llama3)
+        self.ws_bytes = lnk.lnk_paged_workspace_size(self.desc, max(1, w.B))
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.s_handle = self.stream.cuda_stream
+        self.inputs = (self.q, self.k, self.v, self.pos, self.table)
+        self.launches_per_step = 1 + (1 if w.P else 0) + (1 if w.B else 0)
+
+    def attend(self, kp, vp, q_src, out_dst, tab):
+        w, lnk = self.w, self.lnk
+        if w.P == 0:
+            lnk.lnk_paged_decode_attn(self.desc, q_src, self.dec_pos, tab, kp, vp, out_dst, w.B, self.ws,
+                                      self.ws_bytes, self.status, self.s_handle)
+        else:
+            lnk.lnk_paged_step_attn(self.desc, q_src, self.ch[0], self.ch[1], self.ch[2], self.dec_pos, tab, kp, vp,
+                                    out_dst, None, None, w.P, w.B, 0, self.ws, self.ws_bytes, self.status,
+                                    self.s_handle)
+
+    def attend_part(self, kp, vp, part):
+        """One kernel of the step's attention call on its own: the decode rows
+        ("decode") or the prompt chunks ("chunk")."""
+        w, lnk = self.w, self.lnk
+        if part == "decode":
+            lnk.lnk_paged_decode_attn(self.desc, self.q_out[w.P:], self.dec_pos, self.table, kp, vp,
+                                      self.out[w.P:], w.B, self.ws, self.ws_bytes, self.status, self.s_handle)
+        else:
+            lnk.lnk_paged_step_attn(self.desc, self.q_out, self.ch[0], self.ch[1], self.ch[2], None, self.table,
+                                    kp, vp, self.out, None, None, w.P, 0, 0, None, 0, self.status, self.s_handle)
+
+    def step(self, i, inp, ev=None, out_dst=None):
+        w = self.w
+        qq, kk, vv, pp, tab = inp
+        kp, vp = self.pools[i % self.copies]
+        self.lnk.lnk_paged_append_rope(self.desc, self.rd, qq, kk, vv, pp, self.rows, None, tab, self.gq, self.gk,
+                                       w.norm_eps, kp, vp, self.q_out, w.T, self.status, self.s_handle)
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.attend(kp, vp, self.q_out, self.out if out_dst is None else out_dst, tab)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def check_status(self):
+        st = int(self.status.item())
+        assert st == 0, f"device status {st:#x}"
+
+    def warm(self, n):
+        with self.torch.cuda.stream(self.stream):
+            for i in range(n):
+                self.step(i, self.inputs)
+        self.stream.synchronize()
+        self.check_status()
+
+    def timed(self, steps, dist=None, sampler=None):
+        """Device time of `steps` whole steps, CUDA events on the launching stream."""
+        torch = self.torch
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_on()
+        with torch.cuda.stream(self.stream):
+            t_start.record(self.stream)
+            for i in range(steps):
+                self.step(i, self.inputs)
+            t_end.record(self.stream)
+        self.stream.synchronize()
+        if sampler:
+            sampler.mark_off()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        return t_start.elapsed_time(t_end)
+
+    def kernel_times(self, n):
+        """Average device time of the attention call and, for steps with both
+        prompt chunks and decode rows, of each of its two kernels alone: events
+        on the launching stream around the call, over n steps of the same
+        workload.  (Events between the append and the attention call would stop
+        the attention kernel from overlapping the append kernel's tail, so the
+        whole-step timing has none.)"""
+        torch, w = self.torch, self.w
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(self.stream):
+            for i in range(n):
+                self.step(i, self.inputs, ev[i])
+        self.stream.synchronize()
+        times = {"attn": sum(a.elapsed_time(b) for a, b in ev) / n}
+        if w.P and w.B:
+            for part in ("decode", "chunk"):
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(n)]
+                with torch.cuda.stream(self.stream):
+                    for i in range(n):
+                        kp, vp = self.pools[i % self.copies]
+                        ev[i][0].record(self.stream)
+                        self.attend_part(kp, vp, part)
+                        ev[i][1].record(self.stream)
+                self.stream.synchronize()
+                times[part] = sum(a.elapsed_time(b) for a, b in ev) / n
+        self.check_status()
+        return times
+
+    def roofline(self, times, config, kt_steps):
+        """The roofline object: the decode kernel against the HBM peak (the
+        step's dominant kernel whenever it has decode rows), or, for prefill
+        alone, the chunk kernel against the tensor peak; for steps with both,
+        the chunk kernel's tensor figure under "chunk"."""
+        w, parts = self.w, self.parts
+        peak, peak_kind = read_peaks()
+        tpeak, tkind = read_tensor_peak()
+        timing = (f"CUDA events around the call on its stream, average over {kt_steps} steps of the same "
+                  "workload right after the timed region")
+        if w.B:
+            dec_ms = times["decode"] if w.P else times["attn"]
+            dec_bytes = parts["decode_call"]
+            achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+            r = {"bound": "hbm", "kernel": "decode_kernel (lnk_paged_decode_attn over the step's decode rows)",
+                 "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                 "traffic": recorded_traffic("decode.cu", config + ("_e4m3" if self.e4m3 else "")),
+                 "algorithmic_bytes": dec_bytes, "avg_launch_ms": round(dec_ms, 5), "timing": timing}
+        if w.P:
+            flops = chunk_flops(w)
+            ch_ms = times["chunk"] if w.B else times["attn"]
+            achieved = flops / (ch_ms / 1e3) / 1e12
+            c = {"bound": "tensor", "kernel": "chunk_kernel (lnk_paged_step_attn over the step's prompt chunks)",
+                 "achieved": round(achieved, 2), "peak": tpeak, "unit": "TFLOP/s",
+                 "frac": round(achieved / tpeak, 4), "peak_source": tkind,
+                 "traffic": recorded_traffic("chunk.cu", config), "algorithmic_flops": flops,
+                 "avg_launch_ms": round(ch_ms, 5), "timing": timing}
+            if not w.B:
+                return c
+            r["chunk"] = c
+            step_bytes = parts["decode_call"] + parts["chunk_kv"] + parts["chunk_q_out"]
+            r["step_attn"] = {"kernels": "chunk_kernel + decode_kernel (one lnk_paged_step_attn call)",
+                              "achieved": round(step_bytes / (times["attn"] / 1e3) / 1e9, 2), "unit": "GB/s",
+                              "frac": round(step_bytes / (times["attn"] / 1e3) / 1e9 / peak, 4),
+                              "algorithmic_bytes": step_bytes, "avg_launch_ms": round(times["attn"], 5)}
+        return r
+
+    def e2e(self, steps, elapsed_ms, dist=None):
+        """End to end through the C ABI: every step's inputs copied from pinned
+        host memory (one packed buffer, one copy), the calls, and the result
+        copied back to pinned host memory.  As a serving loop would, the two
+        copy directions run on their own streams with double buffers, so that
+        step i + 1's inputs and step i - 1's result move while the kernels of
+        step i run.  Returns (ms, h2d bytes, d2h bytes, steps, how)."""
+        torch, w, dev = self.torch, self.w, self.dev
+        host_parts = [w.step_q().view(np.uint8).ravel(), w.step_k().view(np.uint8).ravel(),
+                      w.step_v().view(np.uint8).ravel(), w.token_positions().astype(np.int32).view(np.uint8),
+                      np.ascontiguousarray(w.table, dtype=np.int32).view(np.uint8).ravel()]
+        offs = np.cumsum([0] + [((a.size + 255) // 256) * 256 for a in host_parts])
+        h_in = torch.zeros(int(offs[-1]), dtype=torch.uint8).pin_memory()
+        for a, o0 in zip(host_parts, offs[:-1]):
+            h_in[int(o0):int(o0) + a.size] = torch.from_numpy(a.copy())
+        d_in = [torch.empty_like(h_in, device=dev) for _ in range(2)]
+
+        def views(sl):
+            def view(i, dtype, shape):
+                n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+                return d_in[sl][int(offs[i]):int(offs[i]) + n].view(dtype).view(shape)
+            return (view(0, torch.int16, self.q.shape), view(1, torch.int16, self.k.shape),
+                    view(2, torch.int16, self.v.shape), view(3, torch.int32, self.pos.shape),
+                    view(4, torch.int32, self.table.shape))
+
+        e_inputs = [views(0), views(1)]
+        d_out = [torch.zeros_like(self.out) for _ in range(2)]
+        h_out = [torch.empty(self.out.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
+        h2d = int(sum(a.size for a in host_parts))
+        d2h = h_out[0].numel() * h_out[0].element_size()
+        stream = self.stream
+        up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot copied in
+        ev_done = [torch.cuda.Event() for _ in range(2)]  # the slot's step finished (inputs read, output written)
+        ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's output copied back
+        # Short steps are bound by the host's calls, not the copies: there the
+        # plain loop (copies and kernels in order on one stream) is faster.
+        pipelined = elapsed_ms > 0.05
+
+        def run(n):
+            if not pipelined:
+                with torch.cuda.stream(stream):
+                    for i in range(n):
+                        d_in[0].copy_(h_in, non_blocking=True)
+                        self.step(i, e_inputs[0], out_dst=d_out[0])
+                        h_out[0].copy_(d_out[0], non_blocking=True)
+                return
+            for i in range(n):
+                sl = i & 1
+                with torch.cuda.stream(up_stream):
+                    if i >= 2:
+                        up_stream.wait_event(ev_done[sl])
+                    d_in[sl].copy_(h_in, non_blocking=True)
+                    ev_in[sl].record(up_stream)
+                stream.wait_event(ev_in[sl])
+                if i >= 2:
+                    stream.wait_event(ev_back[sl])
+                with torch.cuda.stream(stream):
+                    self.step(i, e_inputs[sl], out_dst=d_out[sl])
+                    ev_done[sl].record(stream)
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(ev_done[sl])
+                    h_out[sl].copy_(d_out[sl], non_blocking=True)
+                    ev_back[sl].record(down_stream)
+
+        run(3)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e0.record(up_stream if pipelined else stream)
+        run(steps)
+        e1.record(down_stream if pipelined else stream)
+        torch.cuda.synchronize()
+        self.check_status()
+        last = (steps - 1) & 1 if pipelined else 0
+        assert np.array_equal(h_out[last].numpy(), self.out.cpu().numpy()), \
+            "end-to-end result differs from the device result"
+        how = ("every step: inputs host->device and result device->host (pinned), each direction on its own "
+               "stream overlapping the kernels of the neighbouring steps (double buffers)" if pipelined else
+               "every step: inputs host->device, the kernels and the result device->host (pinned), in order "
+               "on one stream")
+        return e0.elapsed_time(e1), h2d, d2h, how
+
+
 def run_gpu(args, rank, world, dist):
     import torch
 
-    import paged_kv_gqa_row_gb300 as lnk
     import synth
-    from synth import device as sdev
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    seed = None if rank == 0 else 1000 + 97 * rank + synth.WORKLOADS[args.config]
-    w = synth.build(args.config, seed=seed, scale=args.scale, rows=args.rows)
-    e4m3 = args.kv == "e4m3"
-    if e4m3 and w.P:
-        raise SystemExit("--kv e4m3: chunk attention runs on bf16 pools only; use a decode workload")
-    kv_bytes = 1 if e4m3 else 2
-    parts = algorithmic_bytes(w, kv_bytes)
-    pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * kv_bytes
-    copies = args.pool_copies or (2 if pool_bytes < (8 << 30) else 1)
 
-    def d16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    def rank_workload(name, scale, rows):
+        seed = None if rank == 0 else 1000 + 97 * rank + synth.WORKLOADS[name]
+        return synth.build(name, seed=seed, scale=scale, rows=rows)
 
-    def d32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
-
-    shape = (w.hkv, w.pool_positions, w.head_dim)
-    pools = []
-    for _ in range(copies):
-        kp = torch.empty(shape, dtype=torch.uint8 if e4m3 else torch.int16, device=dev)
-        vp = torch.empty_like(kp)
-        fill = sdev.fill_e4m3 if e4m3 else sdev.fill_normal_bf16
-        fill(kp, w.pool_key("k"))
-        fill(vp, w.pool_key("v"))
-        pools.append((kp, vp))
-    q, k, v = d16(w.step_q()), d16(w.step_k()), d16(w.step_v())
-    pos, rows, table = d32(w.token_positions()), d32(w.token_rows()), d32(w.table)
-    dec_pos = d32(w.dec_positions)
-    ch = (d32(w.ch_rows), d32(w.ch_positions), d32(w.ch_segments)) if w.P else (None, None, None)
-    gq = None if w.gamma_q() is None else d16(w.gamma_q())
-    gk = None if w.gamma_k() is None else d16(w.gamma_k())
-    q_out = torch.zeros_like(q)
-    out = torch.zeros_like(q)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row, window=w.window,
-                         kv_dtype=lnk.KV_E4M3 if e4m3 else lnk.KV_BF16, k_scale=K_SCALE_E4M3,
-                         v_scale=V_SCALE_E4M3)
-    rd = lnk.rope_desc(w.theta, w.llama3)
-    ws_bytes = lnk.lnk_paged_workspace_size(desc, max(1, w.B))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    s_handle = stream.cuda_stream
-    row_elems = w.hq * w.head_dim
-
-    def attend(kp, vp, q_src, out_dst, tab):
-        if w.P == 0:
-            lnk.lnk_paged_decode_attn(desc, q_src, dec_pos, tab, kp, vp, out_dst, w.B, ws, ws_bytes,
-                                      status, s_handle)
-        else:
-            lnk.lnk_paged_step_attn(desc, q_src, ch[0], ch[1], ch[2], dec_pos, tab, kp, vp, out_dst,
-                                    None, None, w.P, w.B, 0, ws, ws_bytes, status, s_handle)
-
-    def step(i, inp, ev=None, out_dst=None):
-        qq, kk, vv, pp, tab = inp
-        kp, vp = pools[i % copies]
-        lnk.lnk_paged_append_rope(desc, rd, qq, kk, vv, pp, rows, None, tab, gq, gk, w.norm_eps, kp, vp,
-                                  q_out, w.T, status, s_handle)
-        if ev is not None:
-            ev[0].record(stream)
-        attend(kp, vp, q_out, out if out_dst is None else out_dst, tab)
-        if ev is not None:
-            ev[1].record(stream)
-
-    inputs = (q, k, v, pos, table)
-    launches_per_step = 1 + (1 if w.P else 0) + (1 if w.B else 0)
-
-    # warm-up
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i, inputs)
-    stream.synchronize()
-    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+    w = rank_workload(args.config, args.scale, args.rows)
+    g = GpuWorkload(args, w, dev, args.kv)
+    g.warm(args.warmup)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark_on()
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(i, inputs)
-        t_end.record(stream)
-    stream.synchronize()
-    if sampler:
-        sampler.mark_off()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    # Kernel time for the roofline: the same steps again, with events around the
-    # attention call.  (Events between the append and the attention call would
-    # stop the attention kernel from overlapping the append kernel's tail, so the
-    # main timed region above has none.)
+    elapsed_ms = g.timed(args.steps, dist, sampler)
     kt_steps = max(1, min(args.steps, 500))
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(kt_steps)]
-    with torch.cuda.stream(stream):
-        for i in range(kt_steps):
-            step(i, inputs, dec_events[i])
-    stream.synchronize()
-    dec_ms = [a.elapsed_time(b) for a, b in dec_events]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    times = g.kernel_times(kt_steps)
     clocks = sampler.stop() if sampler else None
-
-    # ---- end to end: every step's inputs copied from pinned host memory (one
-    # packed buffer, one copy), the C ABI calls, and the result copied back to
-    # pinned host memory.  As a serving loop would, the two copy directions
-    # run on their own streams with double buffers, so that step i + 1's inputs
-    # and step i - 1's result move while the kernels of step i run. ----
-    host_parts = [w.step_q().view(np.uint8).ravel(), w.step_k().view(np.uint8).ravel(),
-                  w.step_v().view(np.uint8).ravel(), w.token_positions().astype(np.int32).view(np.uint8),
-                  np.ascontiguousarray(w.table, dtype=np.int32).view(np.uint8).ravel()]
-    offs = np.cumsum([0] + [((a.size + 255) // 256) * 256 for a in host_parts])
-    h_in = torch.zeros(int(offs[-1]), dtype=torch.uint8).pin_memory()
-    for a, o0 in zip(host_parts, offs[:-1]):
-        h_in[int(o0):int(o0) + a.size] = torch.from_numpy(a.copy())
-    d_in = [torch.empty_like(h_in, device=dev) for _ in range(2)]
-
-    def views(sl):
-        def view(i, dtype, shape):
-            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-            return d_in[sl][int(offs[i]):int(offs[i]) + n].view(dtype).view(shape)
-        return (view(0, torch.int16, q.shape), view(1, torch.int16, k.shape), view(2, torch.int16, v.shape),
-                view(3, torch.int32, pos.shape), view(4, torch.int32, table.shape))
-
-    e_inputs = [views(0), views(1)]
-    d_out = [torch.zeros_like(out) for _ in range(2)]
-    h_out = [torch.empty(out.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
-    h2d = int(sum(a.size for a in host_parts))
-    d2h = h_out[0].numel() * h_out[0].element_size()
     e2e_steps = max(1, min(args.steps, 200))
-    up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot copied in
-    ev_done = [torch.cuda.Event() for _ in range(2)]  # the slot's step finished (inputs read, output written)
-    ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's output copied back
+    e2e_ms, h2d, d2h, e2e_how = g.e2e(e2e_steps, elapsed_ms / args.steps, dist)
 
-    # Short steps are bound by the host's calls, not the copies: there the
-    # plain loop (copies and kernels in order on one stream) is faster.
-    pipelined = elapsed_ms / args.steps > 0.05
-
-    def e2e_run(n):
-        if not pipelined:
-            with torch.cuda.stream(stream):
-                for i in range(n):
-                    d_in[0].copy_(h_in, non_blocking=True)
-                    step(i, e_inputs[0], out_dst=d_out[0])
-                    h_out[0].copy_(d_out[0], non_blocking=True)
-            return
-        for i in range(n):
-            sl = i & 1
-            with torch.cuda.stream(up_stream):
-                if i >= 2:
-                    up_stream.wait_event(ev_done[sl])
-                d_in[sl].copy_(h_in, non_blocking=True)
-                ev_in[sl].record(up_stream)
-            stream.wait_event(ev_in[sl])
-            if i >= 2:
-                stream.wait_event(ev_back[sl])
-            with torch.cuda.stream(stream):
-                step(i, e_inputs[sl], out_dst=d_out[sl])
-                ev_done[sl].record(stream)
-            with torch.cuda.stream(down_stream):
-                down_stream.wait_event(ev_done[sl])
-                h_out[sl].copy_(d_out[sl], non_blocking=True)
-                ev_back[sl].record(down_stream)
-
-    e2e_run(3)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    e0.record(up_stream if pipelined else stream)
-    e2e_run(e2e_steps)
-    e1.record(down_stream if pipelined else stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
-    last = (e2e_steps - 1) & 1 if pipelined else 0
-    assert np.array_equal(h_out[last].numpy(), out.cpu().numpy()), "end-to-end result differs from the device result"
-
-    vals = torch.tensor([elapsed_ms, e2e_ms, dec_avg_ms], dtype=torch.float64, device=dev)
+    keys = ["elapsed", "e2e"] + sorted(times)
+    vals = torch.tensor([elapsed_ms, e2e_ms] + [times[k] for k in sorted(times)], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms, dec_avg_ms = [float(x) for x in vals.tolist()]
+    got = dict(zip(keys, [float(x) for x in vals.tolist()]))
+    elapsed_ms, e2e_ms = got["elapsed"], got["e2e"]
+    times = {k: got[k] for k in times}
+
+    # the Mistral-shaped decode step, in the same process, when the main
+    # workload is the Llama step (the two long-context configurations)
+    extra = None
+    if args.config == "llama_step" and not args.no_extra and args.kv == "bf16":
+        wm = rank_workload("mistral", 1.0, None)
+        gm = GpuWorkload(args, wm, dev, "bf16")
+        gm.warm(args.warmup)
+        m_ms = gm.timed(args.steps, dist)
+        m_times = gm.kernel_times(kt_steps)
+        vals = torch.tensor([m_ms, m_times["attn"]], dtype=torch.float64, device=dev)
+        if dist:
+            dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+        m_ms, m_times["attn"] = [float(x) for x in vals.tolist()]
+        m_step = gm.parts["step"]
+        extra = {"workload": "mistral", "description": CONFIGS["mistral"],
+                 "value": round(world * m_step * args.steps / (m_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                 "ms_per_step": round(m_ms / args.steps, 5),
+                 "row_steps_per_s": round(world * wm.B * args.steps / (m_ms / 1e3), 1),
+                 "algorithmic_bytes_per_step": m_step,
+                 "l2": f"inputs larger than L2: {gm.copies} pool copies of {gm.pool_bytes / 1e9:.2f} GB, "
+                       "alternated step to step",
+                 "roofline": gm.roofline(m_times, "mistral", kt_steps)}
+        del gm
 
     if rank != 0:
         return None
-    peak, peak_kind = read_peaks()
-    step_bytes = parts["step"]
+    peak, _ = read_peaks()
+    step_bytes = g.parts["step"]
     value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
     e2e_value = world * step_bytes * e2e_steps / (e2e_ms / 1e3) / 1e9
-    dec_bytes = parts["decode_call"] + (parts["chunk_kv"] + parts["chunk_q_out"] if w.P else 0)
-    if w.B:  # decode rows dominate: HBM bound
-        achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm",
-                    "kernel": ("lnk_paged_step_attn (chunk_kernel + decode_kernel)" if w.P
-                               else "lnk_paged_decode_attn (decode_kernel)"),
-                    "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                    "traffic": recorded_traffic("decode.cu", args.config + ("_e4m3" if e4m3 else "")),
-                    "algorithmic_bytes": dec_bytes}
-    else:  # prefill alone: the chunk kernel's contractions, tensor bound
-        flops = chunk_flops(w)
-        tpeak, tkind = read_tensor_peak()
-        achieved = flops / (dec_avg_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "lnk_paged_step_attn (chunk_kernel)",
-                    "achieved": round(achieved, 2), "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": round(achieved / tpeak, 4), "peak_source": tkind,
-                    "traffic": recorded_traffic("chunk.cu", args.config), "algorithmic_flops": flops}
-    roofline["avg_launch_ms"] = round(dec_avg_ms, 5)
-    roofline["timing"] = (f"CUDA events around the attention call on its stream, {kt_steps} steps "
-                          "of the same workload right after the timed region")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if g.e4m3 else "bf16", "data": "synthetic",
         "config": {"workload": args.config, "description": CONFIGS[args.config], "kv_dtype": args.kv,
                    "scale": args.scale, "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.head_dim, "page_size": 64, "num_pages": w.num_pages,
                    "parallelism": f"rows x{world} (independent batches per GPU)",
-                   "l2": f"inputs larger than L2: {copies} pool copies of {pool_bytes / 1e9:.2f} GB, "
+                   "l2": f"inputs larger than L2: {g.copies} pool copies of {g.pool_bytes / 1e9:.2f} GB, "
                          "alternated step to step",
                    "algorithmic_bytes_per_step": step_bytes},
         "row_steps_per_s": round(world * w.B * args.steps / (elapsed_ms / 1e3), 1),
         "chunk_tokens_per_s": round(world * w.P * args.steps / (elapsed_ms / 1e3), 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "roofline": roofline,
+        "roofline": g.roofline(times, args.config, kt_steps),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": ("every step: inputs host->device and result device->host (pinned), each direction "
-                           "on its own stream overlapping the kernels of the neighbouring steps (double buffers)"
-                           if pipelined else "every step: inputs host->device, the kernels and the result "
-                           "device->host (pinned), in order on one stream")},
-        "gpu_launches": launches_per_step * args.steps,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "copies": e2e_how},
+        "gpu_launches": g.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if extra is not None:
+        line["mistral"] = extra
     if not args.no_cpu_baseline:
-        rows_s = sample_tokens(w, args.ref_rows)
-        secs, nb, reps = 0.0, 0, 0
+        units = sample_units(w, args.ref_rows)
+        prepared = prepare_oracle_sample(w, units, kv=args.kv)
+        secs = cpu = 0.0
+        nb, reps = 0, 0
         while secs < args.cpu_seconds and reps < 50:
-            s, b = cpu_oracle_sample(w, rows_s, kv=args.kv)
+            s, c, b = run_oracle_sample(w, prepared, kv=args.kv)
             secs += s
+            cpu += c
             nb += b
             reps += 1
-        line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": threads_used(),
+        what = "decode rows" if w.B else "chunk tokens"
+        line["cpu_baseline"] = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": round(cpu / secs, 2),
                                 "kind": "oracle",
-                                "sample": f"{len(rows_s)} {'decode rows' if w.B else 'chunk tokens'} x {reps} "
-                                          f"repeats of the {args.config} workload ({secs:.1f} s)"}
+                                "sample": f"all kv heads of {len(units) // w.hkv} seeded {what} x {reps} repeats "
+                                          f"of the {args.config} workload ({secs:.1f} s); cores = process CPU "
+                                          "time / wall time"}
     return line
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="mistral", choices=sorted(CONFIGS))
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama_step", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="lnk", choices=["lnk", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
                     help="pool element type (e4m3: 8-bit pools, decode workloads only)")
-    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--ref-rows", type=int, default=4, help="step tokens sampled for the oracle timings")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: about this many seconds of oracle work over all timed steps")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the Mistral line of the default run")
     ap.add_argument("--pool-copies", type=int, default=0, help="pool copies alternated step to step (0: auto)")
     ap.add_argument("--scale", type=float, default=1.0, help="shrink context lengths (profiling runs only)")
     ap.add_argument("--rows", type=int, default=None, help="override the number of decode rows (profiling runs only)")
@@ -604,7 +749,6 @@ def main():
         tdist.init_process_group(backend)
         dist = tdist
     if args.impl == "reference":
-        args.steps = min(args.steps, 10)
         line = run_reference(args, rank, world)
     else:
         line = run_gpu(args, rank, world, dist)

@@ -254,11 +254,15 @@ lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_rope
  *
  * The first call on a device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Each call first clears the array's counters on `stream`
- * (cudaMemsetAsync), then runs the same kernel as lnk_paged_decode_attn.  All
- * calls share the one array: calls that may run at the same time on the GPU
- * (different streams or host threads) race and must be ordered by the caller.
- * Arguments, layouts and errors are otherwise those of lnk_paged_decode_attn.
+ * any stream capture.  A failed lookup returns LNK_ECUDA and is retried by the
+ * next call.  Once its arguments have passed every check, a call clears the
+ * array's counters on `stream` (cudaMemsetAsync) and then runs the same kernel
+ * as lnk_paged_decode_attn; a call that returns an error enqueues nothing.
+ * All calls share the one array: calls that may run at the same time on the
+ * GPU (different streams or host threads) race and must be ordered by the
+ * caller.  Arguments, layouts and errors are otherwise those of
+ * lnk_paged_decode_attn (a descriptor that lnk_paged_workspace_size rejects
+ * gives LNK_EINVAL).
  */
 lnk_status lnk_paged_decode_attn_static(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
                                         const int32_t* positions, const int32_t* table,

@@ -323,10 +323,13 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
 }
 
 // The pools reach the kernel through their tensor maps (kmap, vmap).
+// clear_counters: zero the workspace's counters on the stream right before the
+// launch (after every check has passed), for a workspace whose previous
+// contents are unknown.
 static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, const int32_t* positions,
                                 const int32_t* table, lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes,
                                 int32_t* dev_status, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool clear_counters = false) {
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
@@ -355,13 +358,18 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.window = desc->window;
   p.scale_log2 = scale_log2(desc);
   p.out_scale = kv8 ? desc->v_scale : 1.f;
+  if (clear_counters && cudaMemsetAsync(ws, 0, w.ml, stream) != cudaSuccess) return LNK_ECUDA;
   return launch_decode(kmap, vmap, p, desc->head_dim, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
 }
 
-lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
-                                 const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
-                                 lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                                 lnk_stream stream) {
+}  // extern "C"
+
+namespace lnk {
+
+lnk_status decode_entry(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
+                        const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool, lnk_bf16* out,
+                        int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status, lnk_stream stream,
+                        bool clear_counters) {
   lnk_status st = check_desc(desc);
   if (st != LNK_OK) return st;
   if (B < 0 || B > desc->num_rows) return LNK_EINVAL;
@@ -372,7 +380,19 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
   CUtensorMap kmap, vmap;
   if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
   return decode_common(desc, q_roped, positions, table, out, B, workspace, ws_bytes, dev_status, kmap, vmap,
-                       reinterpret_cast<cudaStream_t>(stream));
+                       reinterpret_cast<cudaStream_t>(stream), clear_counters);
+}
+
+}  // namespace lnk
+
+extern "C" {
+
+lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
+                                 const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool,
+                                 lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 lnk_stream stream) {
+  return decode_entry(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
+                      stream, false);
 }
 
 lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* rows,

@@ -72,6 +72,14 @@ constexpr int kChunksPerCta = 4;  // decode work chunks per persistent CTA
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
 cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch);
+
+// lnk_paged_decode_attn with an option: clear_counters zeroes the workspace's
+// counters on the stream once every argument check has passed, right before
+// the launch (for a workspace whose previous contents are unknown).
+lnk_status decode_entry(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* positions,
+                        const int32_t* table, const lnk_bf16* k_pool, const lnk_bf16* v_pool, lnk_bf16* out,
+                        int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status, lnk_stream stream,
+                        bool clear_counters);
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           int head_dim, const DecodeLaunch& launch, cudaStream_t stream);
 

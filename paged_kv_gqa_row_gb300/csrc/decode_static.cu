@@ -13,11 +13,15 @@
 // the device address is obtained with cudaGetSymbolAddress, once per device,
 // on the first call made while that device is current; that first call makes
 // a runtime call of its own and should therefore come before any stream
-// capture.  Every call shares the array and finds the previous call's data in
-// it: the counters the decode kernel needs at zero are cleared on the stream
-// at the start of every call, and calls whose work overlaps on the GPU (other
-// streams, other host threads) race on the array and must be serialised by the
-// caller.  The call then runs the ordinary decode path on the array.
+// capture.  Only a successful lookup is kept: after a failed one the call
+// returns LNK_ECUDA and the next call on that device tries again.  Every call
+// shares the array and finds the previous call's data in it: the counters the
+// decode kernel needs at zero are cleared on the stream once the call's
+// arguments have passed every check, right before the launch (a call that
+// returns an error enqueues nothing), and calls whose work overlaps on the
+// GPU (other streams, other host threads) race on the array and must be
+// serialised by the caller.  The call then runs the ordinary decode path on
+// the array.
 #include <mutex>
 
 #include "common.cuh"
@@ -34,22 +38,24 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu;
 
-// Device address of the array on the current device (set up on first use).
+// Device address of the array on the current device (looked up on first use;
+// a failed lookup is not remembered).
 cudaError_t scratch_address(void** ptr) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_decode_scratch);
+    err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (err != cudaSuccess) return err;
     g_scratch_ptr[dev] = p;
-  });
+  }
   *ptr = g_scratch_ptr[dev];
-  return g_scratch_err[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -66,13 +72,8 @@ extern "C" lnk_status lnk_paged_decode_attn_static(const lnk_attn_desc* desc, co
   if (need > lnk::kStaticScratchBytes) return LNK_ERANGE;
   void* scratch = nullptr;
   if (lnk::scratch_address(&scratch) != cudaSuccess || scratch == nullptr) return LNK_ECUDA;
-  // the counters at the start of the workspace (chunk claims, per-pair
-  // segments) start at zero
-  const size_t counters =
-      lnk::decode_workspace_layout(B, desc->num_kv_heads, desc->num_q_heads / desc->num_kv_heads, desc->head_dim, 0)
-          .ml;
-  if (cudaMemsetAsync(scratch, 0, counters, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return LNK_ECUDA;
-  return lnk_paged_decode_attn(desc, q_roped, positions, table, k_pool, v_pool, out, B, scratch,
-                               lnk::kStaticScratchBytes, dev_status, stream);
+  // the same checks and launch as lnk_paged_decode_attn, with the workspace's
+  // counters (chunk claims, per-pair segments) zeroed just before the launch
+  return lnk::decode_entry(desc, q_roped, positions, table, k_pool, v_pool, out, B, scratch,
+                           lnk::kStaticScratchBytes, dev_status, stream, true);
 }

@@ -108,6 +108,31 @@ def normal_bf16(key: int, start: int, count: int) -> np.ndarray:
     return f32_to_bf16_bits(normal_f32(key, start, count))
 
 
+def gauss_bf16(key: int, start: int, count: int) -> np.ndarray:
+    """bf16 bits of ``count`` standard normal values with their tails (host only).
+
+    Value i is Box-Muller (Box & Muller, 1958) on SplitMix64 outputs 2i and 2i+1
+    started at ``key``: ``u1 = (h_2i >> 11) + 1`` and ``u2 = h_2i+1 >> 11``, both
+    times 2^-53, ``z = sqrt(-2 ln u1) cos(2 pi u2)`` in float64, rounded to bf16
+    through float32.  |z| reaches about 8.6, unlike the bounded Irwin-Hall values.
+    """
+    h = splitmix64(key, 2 * start, 2 * count).reshape(count, 2)
+    u1 = ((h[:, 0] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+    u2 = (h[:, 1] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+    return f32_to_bf16_bits(z.astype(np.float32))
+
+
+def scale_bf16_pow2(bits: np.ndarray, factor: float) -> np.ndarray:
+    """bf16 bits times a power of two (exact while the result stays normal and finite)."""
+    m, e = math.frexp(float(factor))
+    if factor <= 0 or m != 0.5:
+        raise ValueError("factor must be a power of two")
+    if factor == 1.0:
+        return bits
+    return f32_to_bf16_bits(bf16_bits_to_f32(bits) * np.float32(factor))
+
+
 def e4m3_codes(key: int, start: int, count: int) -> np.ndarray:
     """Bytes for a prefilled 8-bit (E4M3) pool: from SplitMix64 output i, the
     sign is bit 63, the exponent field 4 + (bits 8.. mod 6) and the mantissa
@@ -165,6 +190,11 @@ class Workload:
     ch_segments: np.ndarray  # int32 [P]
     dump_page: int = -1
     norm_eps: float = 1e-6
+    # input shaping for edge cases (no attention arithmetic):
+    dist: str = "ih"            # "ih": Irwin-Hall values (host and device); "gauss": Box-Muller (host only)
+    q_scale: float = 1.0        # power of two multiplying the step's queries
+    k_page_scale: Optional[dict] = None  # physical page -> power of two multiplying its K values
+    gamma_halves: Optional[tuple] = None  # QK-norm gamma (a, b): a on the first half of D, b on the second
 
     @property
     def B(self) -> int:
@@ -197,20 +227,44 @@ class Workload:
         return np.concatenate([self.ch_rows, np.arange(self.B, dtype=np.int32)]).astype(np.int32)
 
     # -- tensors -----------------------------------------------------------
+    @property
+    def device_fillable(self) -> bool:
+        """The pool can be filled on the device (``synth/fill.cu``): Irwin-Hall
+        values with no page scaling."""
+        return self.dist == "ih" and not self.k_page_scale
+
+    def _values(self, key: int, start: int, count: int) -> np.ndarray:
+        if self.dist == "gauss":
+            return gauss_bf16(key, start, count)
+        return normal_bf16(key, start, count)
+
+    def _tensor(self, stream: int, shape) -> np.ndarray:
+        n = int(np.prod(shape)) if len(shape) else 1
+        return self._values(stream_key(self.seed, stream), 0, n).reshape(shape)
+
     def step_q(self) -> np.ndarray:
-        return tensor_bf16(self.seed, STREAM_Q, (self.T, self.hq, self.head_dim))
+        return scale_bf16_pow2(self._tensor(STREAM_Q, (self.T, self.hq, self.head_dim)), self.q_scale)
 
     def step_k(self) -> np.ndarray:
-        return tensor_bf16(self.seed, STREAM_K_NEW, (self.T, self.hkv, self.head_dim))
+        return self._tensor(STREAM_K_NEW, (self.T, self.hkv, self.head_dim))
 
     def step_v(self) -> np.ndarray:
-        return tensor_bf16(self.seed, STREAM_V_NEW, (self.T, self.hkv, self.head_dim))
+        return self._tensor(STREAM_V_NEW, (self.T, self.hkv, self.head_dim))
+
+    def _gamma(self, stream: int) -> Optional[np.ndarray]:
+        if not self.qk_norm:
+            return None
+        if self.gamma_halves is not None:
+            a, b = self.gamma_halves
+            h = self.head_dim // 2
+            return f32_to_bf16_bits(np.array([a] * h + [b] * h, dtype=np.float32))
+        return gamma_bf16(self.seed, stream, self.head_dim)
 
     def gamma_q(self) -> Optional[np.ndarray]:
-        return gamma_bf16(self.seed, STREAM_GAMMA_Q, self.head_dim) if self.qk_norm else None
+        return self._gamma(STREAM_GAMMA_Q)
 
     def gamma_k(self) -> Optional[np.ndarray]:
-        return gamma_bf16(self.seed, STREAM_GAMMA_K, self.head_dim) if self.qk_norm else None
+        return self._gamma(STREAM_GAMMA_K)
 
     def pool_key(self, which: str) -> int:
         return stream_key(self.seed, STREAM_K_POOL if which == "k" else STREAM_V_POOL)
@@ -218,8 +272,13 @@ class Workload:
     def pool(self, which: str) -> np.ndarray:
         """The whole initial pool ``[Hkv, num_pages*64, D]`` (small workloads only)."""
         n = self.hkv * self.pool_positions * self.head_dim
-        return normal_bf16(self.pool_key(which), 0, n).reshape(
+        out = self._values(self.pool_key(which), 0, n).reshape(
             self.hkv, self.pool_positions, self.head_dim)
+        if which == "k" and self.k_page_scale:
+            for pg, f in self.k_page_scale.items():
+                sl = slice(int(pg) * PAGE_SIZE, (int(pg) + 1) * PAGE_SIZE)
+                out[:, sl] = scale_bf16_pow2(out[:, sl], f)
+        return out
 
     def pool_e4m3(self, which: str) -> np.ndarray:
         """The whole 8-bit pool [Hkv][num_pages * 64][D] of codes (prefilled context)."""
@@ -242,7 +301,9 @@ class Workload:
         out = np.empty((len(pages), PAGE_SIZE, self.head_dim), dtype=np.uint16)
         for i, pg in enumerate(np.asarray(pages, dtype=np.int64)):
             start = (kv_head * self.pool_positions + int(pg) * PAGE_SIZE) * self.head_dim
-            out[i] = normal_bf16(key, start, per_page).reshape(PAGE_SIZE, self.head_dim)
+            out[i] = self._values(key, start, per_page).reshape(PAGE_SIZE, self.head_dim)
+            if which == "k" and self.k_page_scale and int(pg) in self.k_page_scale:
+                out[i] = scale_bf16_pow2(out[i], self.k_page_scale[int(pg)])
         return out
 
     def visible_keys(self) -> int:

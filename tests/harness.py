@@ -40,14 +40,16 @@ def to_bits(t) -> np.ndarray:
 class DeviceStep:
     """Device buffers of one workload step and the library calls on them."""
 
-    def __init__(self, w: synth.Workload, fill: str = "auto", device="cuda"):
+    def __init__(self, w: synth.Workload, fill: str = "auto", device="cuda", scale: float = 0.0):
         import torch
         import paged_kv_gqa_row_gb300 as lnk
         self.w, self.lnk = w, lnk
         shape = (w.hkv, w.pool_positions, w.head_dim)
         n_pool = int(np.prod(shape))
         if fill == "auto":
-            fill = "host" if n_pool <= (1 << 26) else "device"
+            fill = "host" if (n_pool <= (1 << 26) or not w.device_fillable) else "device"
+        if fill == "device" and not w.device_fillable:
+            raise ValueError("this workload's pool can only be filled on the host")
         if fill == "host":
             self.k_pool = _t(w.pool("k"), device)
             self.v_pool = _t(w.pool("v"), device)
@@ -70,7 +72,7 @@ class DeviceStep:
         self.out = torch.zeros((w.T, w.hq, w.head_dim), dtype=torch.int16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows,
-                                  w.pages_per_row, window=w.window)
+                                  w.pages_per_row, window=w.window, scale=scale)
         self.rope = lnk.rope_desc(w.theta, w.llama3)
         self.ws_bytes = max(lnk.lnk_paged_workspace_size(self.desc, max(w.B, 1)), 256)
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
@@ -112,18 +114,19 @@ def oracle_inv(w: synth.Workload) -> np.ndarray:
     return orope.inv_freq(w.theta, w.head_dim, w.llama3)
 
 
-def oracle_full(w: synth.Workload):
-    """Whole-pool oracle (small workloads): (q_out, k_pool, v_pool, out)."""
+def oracle_full(w: synth.Workload, scale=None):
+    """Whole-pool oracle (small workloads): (q_out, k_pool, v_pool, out).
+    ``scale``: the attention scale (None: the default rsqrt(head_dim))."""
     q_out, kp, vp = opaged.append_rope(w.step_q(), w.step_k(), w.step_v(), w.token_positions(),
                                        w.token_rows(), w.table, w.pool("k"), w.pool("v"),
                                        oracle_inv(w), gamma_q=w.gamma_q(), gamma_k=w.gamma_k(),
                                        eps=w.norm_eps)
     out = opaged.step_attention(q_out, w.ch_rows, w.ch_positions, w.dec_positions, w.table, kp, vp,
-                                w.window)
+                                w.window, scale)
     return q_out, kp, vp, out
 
 
-def oracle_tokens(w: synth.Workload, tokens) -> dict:
+def oracle_tokens(w: synth.Workload, tokens, scale=None) -> dict:
     """Oracle outputs of selected step tokens (index into the P + B tokens),
     computed on a compact pool holding only the pages those tokens read."""
     tp, tr = w.token_positions(), w.token_rows()
@@ -159,7 +162,7 @@ def oracle_tokens(w: synth.Workload, tokens) -> dict:
         ctable = np.full((1, lps[-1] + 1), -1, dtype=np.int32)
         ctable[0, lps] = np.arange(len(lps), dtype=np.int32)
         q_t = q_out[writers.index(t)]
-        results[t] = opaged.attention_at(q_t, 0, p, ctable, kp2, vp2, w.window)
+        results[t] = opaged.attention_at(q_t, 0, p, ctable, kp2, vp2, w.window, scale)
     return results
 
 
