@@ -1,36 +1,42 @@
 // K4: packed prompt chunks (prefill_paged / the prompt part of step_paged) on
-// the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+// the fifth-generation tensor cores, two SMs per tile (tcgen05 cta_group::2,
+// accumulators in tensor memory).
 //
 // Every chunk token attends over its own row's pages up to its position (and
-// the window).  A CTA takes one tile of consecutive pack tokens and one kv
-// head: 256 / G tokens times the G query heads of that kv head, i.e. 256
-// query rows (row m = token * G + head) in two halves of 128 rows; each half
-// owns the 128 tensor-memory lanes in its own 256 columns.  Tokens of a tile
-// are grouped into runs of equal table rows; for each run the pages covering
-// the run's key range are streamed through the kernel once, for both halves.
+// the window).  A tile is 256 / G consecutive pack tokens times the G query
+// heads of one kv head: 256 query rows (row m = token * G + head).  A cluster
+// of two CTAs takes one tile: CTA rank r owns rows 128 r .. 128 r + 127 in its
+// tensor-memory lanes.  Tokens of a tile are grouped into runs of equal table
+// rows; the pages covering each run's key range are streamed once, two pages
+// (128 keys) per step, for all 256 rows.
 //
-// CTA structure (320 threads, warp-specialised):
-//  * warp 0, producer: loads each page's K and V (2-D TMA boxes, 128-byte
-//    swizzle) into a ring of stages;
-//  * warp 1, MMA: one thread issues, per page j and half h,
-//      S_h[128 x 64]  = Q_h K_j^T        (tcgen05.mma; Q_h from tensor memory,
-//                                         K_j K-major in shared memory)
-//      O_h[128 x D]  += P_h V_j          (P from tensor memory as bf16, written
-//                                         over the first 32 columns of S_h;
-//                                         V_j MN-major in shared memory)
-//    in the order P.V of half 0, Q.K of half 0 for the next page, then the
-//    same for half 1: while the softmax of one half works on a page the
-//    tensor core serves the other half (ping-pong).  The products issued by
-//    one thread run in order, so Q.K of the next page overwrites S_h only
-//    after P.V has read P from it.  With Q in tensor memory a Q.K product
-//    reads only K from shared memory;
-//  * warps 2-9, softmax, four per half: thread r of a half owns query row r
-//    (tensor-memory lane r).  It first writes its query row into tensor
-//    memory; then, per page, it reads its 64 scores, masks them (same run,
-//    lo <= key <= position), updates the running max and sum in registers,
-//    writes P back to tensor memory, and rescales its row of O only when the
-//    running max grows by more than 2^8 (until then P stays below 256, exact
-//    enough in bf16); at the end it normalises its row of O and stores it.
+// Products are 2-SM (M = 256) and issued by one thread of rank 0:
+//   S_b[256 x 128] = Q K_j^T   Q from each CTA's tensor memory (bf16 pairs),
+//                              K_j K-major in shared memory: rank r holds page
+//                              2j + r of the step (keys 64 r .. 64 r + 63);
+//   O[256 x 128]  += P_b V_j   P from tensor memory (bf16, written over the
+//                              first 64 columns of S_b), V_j MN-major: rank r
+//                              holds head-dim columns 64 r .. 64 r + 63 of both
+//                              pages.
+// S is double-buffered (b = j mod 2), so Q K^T of step j + 1 runs on the
+// tensor cores while the softmax works on step j.  Products issued by one
+// thread run in order: Q K^T of step j + 2 overwrites S_b only after P V of
+// step j has read P from it.
+//
+// CTA structure (192 threads, warp-specialised, both ranks):
+//  * warp 0, producer: TMA loads of this CTA's K page and V columns into
+//    rings of stages;
+//  * warp 1: in rank 0, the MMA thread; in rank 1, a relay that tells rank 0
+//    when rank 1's stages have landed (rank 0's MMA reads both CTAs' stages);
+//  * warps 2-5, softmax: thread r owns query row r of its CTA (tensor-memory
+//    lane r).  It writes its query row into tensor memory; then, per step,
+//    reads 128 scores, masks them (same run, lo <= key <= position, valid
+//    page), updates the running max and sum in registers, writes P, and
+//    rescales its row of O only when the running max grows by more than 2^8
+//    (until then P stays below 256, exact enough in bf16); at the end it
+//    normalises its row of O and stores it.
+// Barriers that the other CTA arrives on live in rank 0 (the Q, P and
+// relay barriers); the 2-SM commits arrive in both CTAs at once.
 //
 // Sources: "Mistral 7B Instruct v0.3", Entries table (prefill_paged: prompts
 // packed end to end, each token written at its place in the pool and attending
@@ -43,45 +49,72 @@
 namespace lnk {
 namespace {
 
-constexpr int kHalves = kChunkHalves;
-constexpr int kSoftmaxWarps = 4 * kHalves;
-constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
-constexpr int kStages = 4;
-constexpr int kRows = 128;                // query rows per half = tensor-memory lanes
-constexpr int kTileRows = kRows * kHalves;
+constexpr int kThreads = 11 * 32;
+constexpr int kStagesK = 4;               // K ring (this CTA's page of a step)
+constexpr int kStagesV = 4;               // V ring (this CTA's columns of both pages)
+constexpr int kRows = 128;                // query rows per CTA = tensor-memory lanes
+constexpr int kTileRows = 2 * kRows;      // rows of a tile (both CTAs)
+constexpr int kStepKeys = 2 * kPage;      // keys per step
 constexpr float kRescaleLog2 = 8.f;       // rescale O when the max grows by more than 2^8
 constexpr int kMaxOrderedTiles = 512;     // tiles ordered by cost (larger launches keep token order)
-
-struct PageInfo {
-  int run, key_base, valid, pad;
-};
 
 template <int D>
 struct TcSmem {
   static constexpr int NB = boxes_for(D);
-  static constexpr int kStageBytes = 2 * NB * kBoxBytes;    // K boxes, then V boxes
-  static constexpr int kPvN = D <= 64 ? 64 : 128;           // N of the P.V product (D = 96 padded)
+  static constexpr int kKStage = NB * kBoxBytes;            // one page of K, all head-dim columns
+  static constexpr int kVStage = 2 * kBoxBytes;             // both pages of V, 64 head-dim columns
+  static constexpr int kPvN = 128;                          // N of P.V (head_dim padded; 64 per CTA)
   static constexpr uint32_t kTmemCols = 512;
-  // tensor-memory columns of a half (half h adds h * kHalfCols): Q (bf16
-  // pairs), S (P of the page over its first 32 columns), O
-  static constexpr uint32_t kHalfCols = 256;
-  static constexpr uint32_t kColQ = 0, kColS = 64, kColO = 128;
-  static constexpr size_t stages = 0;
-  static constexpr size_t bars = stages + size_t(kStages) * kStageBytes;
-  // full[S], empty[S], q_full, s_full[H], p_full[H], pv_done[H], zero
-  static constexpr int kNumBars = 2 * kStages + 2 + 3 * kHalves;
-  static constexpr size_t info = bars + kNumBars * sizeof(uint64_t);
-  static constexpr size_t tok = info + kStages * sizeof(PageInfo);
+  // tensor-memory columns: S_0, S_1 (f32 scores), P_0, P_1 (bf16 pairs), O
+  static constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+  static constexpr int kQBox = kRows * 128;                 // 128 query rows x 64 head-dim columns
+  static constexpr size_t kring = 0;
+  static constexpr size_t vring = kring + size_t(kStagesK) * kKStage;
+  static constexpr size_t qsm = vring + size_t(kStagesV) * kVStage;  // this CTA's query rows, K-major
+  static constexpr size_t bars = qsm + size_t(NB) * kQBox;
+  // kfull[K], kempty[K], vfull[V], vempty[V], sfull[2], sfree[2], pfull[2], pvdone[2], odone, qfull
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 10;
+  static constexpr size_t tok = bars + kNumBars * sizeof(uint64_t);
   static constexpr size_t runs = tok + 4 * kTileRows * 4;
-  static constexpr size_t misc = runs + 4 * kTileRows * 4;  // [0] runs, [1] pages, [2] abort, [3] tmem base, [4] tile
-  static constexpr size_t cost = misc + 64;                   // [kMaxOrderedTiles] estimated pages per tile
-  static constexpr size_t end = cost + kMaxOrderedTiles * 4;
-  // more than half of the shared memory, so that one CTA holds the tensor memory of an SM
-  static constexpr size_t bytes = (end + 1024) > 120 * 1024 ? (end + 1024) : 120 * 1024;
+  static constexpr size_t misc = runs + 5 * kTileRows * 4;  // [0] runs, [1] steps, [2] abort, [3] tmem, [4] tile
+  static constexpr size_t cost = misc + 64;                 // [kMaxOrderedTiles] estimated pages per tile
+  // softmax groups' hand-off: max [2][128] and ok [2][128] per step parity;
+  // at the end max, sum and ok [2][128] per group
+  static constexpr size_t xchg = cost + kMaxOrderedTiles * 4;
+  static constexpr size_t end = xchg + 10 * kRows * 4;
+  static constexpr size_t bytes = end + 1024;
 };
 
+// Walks the steps of a tile in order: run r, step s of the run (pages
+// first + 2 s and first + 2 s + 1, the second one past the run's last page
+// when the run has an odd number of pages).
+struct StepCursor {
+  int run = 0, s = 0;
+  __device__ __forceinline__ void next(const int* run_steps) {
+    if (++s >= run_steps[run]) {
+      ++run;
+      s = 0;
+    }
+  }
+};
+
+constexpr int kPastRun = -2147483647 - 1;  // "entry" of a page past the end of its run
+
+// Table entries of the two pages of the step at `c` (kPastRun for a page past
+// its run, and for both past the last run).
+__device__ __forceinline__ void step_entries(const ChunkParams& p, const int* run_row, const int* run_first,
+                                             const int* run_kmax, int nruns, const StepCursor& c, int& ea,
+                                             int& eb) {
+  ea = eb = kPastRun;
+  if (c.run >= nruns) return;
+  const int* trow = p.table + static_cast<long long>(run_row[c.run]) * p.pages_per_row;
+  const int lp = run_first[c.run] + 2 * c.s;
+  ea = trow[lp];
+  if (lp + 1 <= (run_kmax[c.run] - 1) / kPage) eb = trow[lp + 1];
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const ChunkParams p) {
   using L = TcSmem<D>;
@@ -89,14 +122,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int DK = D / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* q_full = empty_bar + kStages;
-  uint64_t* s_full = q_full + 1;          // [H]
-  uint64_t* p_full = s_full + kHalves;    // [H]
-  uint64_t* pv_done = p_full + kHalves;   // [H]
-  uint64_t* zero_bar = pv_done + kHalves;
-  PageInfo* info = reinterpret_cast<PageInfo*>(smem + L::info);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* kempty = kfull + kStagesK;
+  uint64_t* vfull = kempty + kStagesK;
+  uint64_t* vempty = vfull + kStagesV;
+  uint64_t* sfull = vempty + kStagesV;   // [2] Q.K^T into S_b finished
+  uint64_t* sfree = sfull + 2;           // [2] the softmax has read S_b (rank 0 only)
+  uint64_t* pfull = sfree + 2;           // [2] P_b written (rank 0 only)
+  uint64_t* pvdone = pfull + 2;          // [2] P.V from P_b finished (all but the last)
+  uint64_t* odone = pvdone + 2;          // the last P.V
+  uint64_t* qfull = odone + 1;           // rank 0 only
   int* tok_lo = reinterpret_cast<int*>(smem + L::tok);
   int* tok_hi = tok_lo + kTileRows;
   int* tok_run = tok_hi + kTileRows;
@@ -104,18 +139,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* run_row = reinterpret_cast<int*>(smem + L::runs);
   int* run_kmin = run_row + kTileRows;
   int* run_kmax = run_kmin + kTileRows;
-  int* run_pages = run_kmax + kTileRows;
+  int* run_first = run_kmax + kTileRows;  // first logical page
+  int* run_steps = run_first + kTileRows;
   int* misc = reinterpret_cast<int*>(smem + L::misc);
   volatile int* abort_flag = misc + 2;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const int cid = static_cast<int>(blockIdx.x >> 1);  // cluster = tile and kv head
   const int G = p.group;
-  const int TQ = kHalves * p.tile_tokens;  // tokens of the tile
-  // Longest tiles first: CTAs are dispatched in launch order, so the CTA of
-  // launch rank L takes the (L / Hkv)-th tile by estimated cost (pages up to
-  // its last position) and kv head L % Hkv.  Every CTA computes the same order.
+  const int TQ = 2 * p.tile_tokens;       // tokens of the tile
+  // Longest tiles first: clusters are dispatched in launch order, so the
+  // cluster of launch rank c takes the (c / Hkv)-th tile by estimated cost
+  // (pages up to its last position) and kv head c % Hkv.  Every CTA computes
+  // the same order.
   int tile, h;
   if (p.num_tiles <= kMaxOrderedTiles) {
     int* cost = reinterpret_cast<int*>(smem + L::cost);
@@ -125,47 +164,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       cost[i] = pm >= 0 ? pm / kPage + 1 : 0;
     }
     __syncthreads();
-    const int rank_wanted = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) / p.hkv;
+    const int rank_wanted = cid / p.hkv;
     for (int i = tid; i < p.num_tiles; i += kThreads) {
       const int ci = cost[i];
-      int rank = 0;
+      int rk = 0;
       for (int k = 0; k < p.num_tiles; ++k) {
         const int ck = cost[k];
-        rank += (ck > ci) || (ck == ci && k > i);  // ties: later tokens first
+        rk += (ck > ci) || (ck == ci && k > i);  // ties: later tokens first
       }
-      if (rank == rank_wanted) misc[4] = i;
+      if (rk == rank_wanted) misc[4] = i;
     }
     __syncthreads();
     tile = misc[4];
-    h = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) % p.hkv;
   } else {
-    tile = p.num_tiles - 1 - static_cast<int>(blockIdx.x);  // later tokens first
-    h = blockIdx.y;
+    tile = p.num_tiles - 1 - cid / p.hkv;  // later tokens first
   }
+  h = cid % p.hkv;
   const int t0 = tile * TQ;
   const int nt = min(TQ, p.P - t0);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_addr(full_bar + s), 1);
-      mbar_init(smem_addr(empty_bar + s), 1);
+    // rank 0's full barriers also count the relay's arrival for rank 1's copy
+    for (int s = 0; s < kStagesK; ++s) {
+      mbar_init(smem_addr(kfull + s), rank == 0 ? 2 : 1);
+      mbar_init(smem_addr(kempty + s), 1);
     }
-    mbar_init(smem_addr(q_full), kSoftmaxWarps);
-    for (int i = 0; i < kHalves; ++i) {
-      mbar_init(smem_addr(s_full + i), 1);
-      mbar_init(smem_addr(p_full + i), 4);
-      mbar_init(smem_addr(pv_done + i), 1);
+    for (int s = 0; s < kStagesV; ++s) {
+      mbar_init(smem_addr(vfull + s), rank == 0 ? 2 : 1);
+      mbar_init(smem_addr(vempty + s), 1);
     }
-    mbar_init(smem_addr(zero_bar), kTileRows);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(sfull + b), 1);
+      mbar_init(smem_addr(sfree + b), 8);   // one softmax group (four warps) in each CTA
+      mbar_init(smem_addr(pfull + b), 8);
+      mbar_init(smem_addr(pvdone + b), 1);
+    }
+    mbar_init(smem_addr(odone), 1);
+    mbar_init(smem_addr(qfull), 8);
     misc[2] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 1) tmem_alloc(smem_addr(misc + 3), L::kTmemCols);
+  if (warp == 1) tmem2_alloc(smem_addr(misc + 3), L::kTmemCols);
   // ---- tokens of the tile ----
-  if (tid < TQ) {
+  for (int i = tid; i < TQ; i += kThreads) {
     int lo = 0, hi = 0, bad = 0, row = -1;
-    if (tid < nt) {
-      const int t = t0 + tid;
+    if (i < nt) {
+      const int t = t0 + i;
       const int pos = p.positions[t];
       row = p.rows[t];
       if (pos >= 0) {
@@ -180,14 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.rows[t] != p.rows[t - 1])
         bad |= LNK_DEV_SEGMENT;
     }
-    tok_lo[tid] = lo;
-    tok_hi[tid] = hi;
-    tok_row[tid] = row;
-    if (bad && h == 0 && p.status != nullptr) atomicOr(p.status, bad);
+    tok_lo[i] = lo;
+    tok_hi[i] = hi;
+    tok_row[i] = row;
+    if (bad && h == 0 && rank == 0 && p.status != nullptr) atomicOr(p.status, bad);
   }
   __syncthreads();
   if (tid == 0) {
-    int nr = 0, cur = -1, pages = 0;
+    int nr = 0, cur = -1, steps = 0;
     for (int i = 0; i < nt; ++i) {
       if (tok_hi[i] <= tok_lo[i]) {
         tok_run[i] = -1;
@@ -207,306 +251,418 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = nt; i < TQ; ++i) tok_run[i] = -1;
     for (int r = 0; r < nr; ++r) {
-      run_pages[r] = (run_kmax[r] - 1) / kPage - run_kmin[r] / kPage + 1;
-      pages += run_pages[r];
+      run_first[r] = run_kmin[r] / kPage;
+      const int pages = (run_kmax[r] - 1) / kPage - run_first[r] + 1;
+      run_steps[r] = (pages + 1) / 2;
+      steps += run_steps[r];
     }
     misc[0] = nr;
-    misc[1] = pages;
+    misc[1] = steps;
   }
+  // barriers initialised and tensor memory allocated in both CTAs before any
+  // thread of either uses them
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
-  const int nruns = misc[0];
-  const int npages = misc[1];
+  const int nsteps = misc[1];
   const uint32_t tmem = static_cast<uint32_t>(misc[3]);
 
   if (warp == 0) {
     // ============================== producer ==============================
-    if (lane == 0 && npages > 0) {
-      int k = 0;
-      bool stop = false;
-      for (int run = 0; run < nruns && !stop; ++run) {
-        const int* trow = p.table + static_cast<long long>(run_row[run]) * p.pages_per_row;
-        const int first = run_kmin[run] / kPage;
-        for (int j = 0; j < run_pages[run]; ++j, ++k) {
-          const int s = k % kStages;
-          if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
-            stop = true;
-            break;
-          }
-          const int lp = first + j;
-          const int page = trow[lp];
-          const uint32_t fb = smem_addr(full_bar + s);
-          PageInfo si{run, lp * kPage, 1, 0};
-          if (page < 0 || page >= p.num_pages) {
-            if (p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
-            si.valid = 0;
-            info[s] = si;
-            mbar_arrive(fb);
-          } else {
-            info[s] = si;
-            mbar_arrive_expect_tx(fb, L::kStageBytes);
-            const uint32_t kdst = smem_addr(smem + L::stages + size_t(s) * L::kStageBytes);
-            const uint32_t vdst = kdst + NB * kBoxBytes;
-            const int y = (h * p.num_pages + page) * kPage;
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              tma_load_2d(kdst + nb * kBoxBytes, &kmap, nb * kBoxCols, y, fb);
-              tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
-            }
-          }
+    if (lane == 0 && nsteps > 0) {
+      StepCursor cur;
+      int ea, eb;  // table entries of the step's two pages, read one step ahead
+      step_entries(p, run_row, run_first, run_kmax, misc[0], cur, ea, eb);
+      int j = 0;
+      for (; j < nsteps; ++j, cur.next(run_steps)) {
+        const int sk = j % kStagesK, sv = j % kStagesV;
+        int na, nb;
+        {
+          StepCursor nc = cur;
+          nc.next(run_steps);
+          step_entries(p, run_row, run_first, run_kmax, misc[0], nc, na, nb);
         }
+        // a page past the run or a bad table entry loads page 0 instead (its
+        // keys are masked and its values zeroed)
+        const bool bad_a = ea >= p.num_pages || ea < 0;
+        const bool bad_b = eb != kPastRun && (eb >= p.num_pages || eb < 0);
+        if (rank == 0 && (bad_a || bad_b) && p.status != nullptr) atomicOr(p.status, LNK_DEV_BAD_PAGE);
+        const int pa = bad_a ? 0 : ea, pb = (bad_b || eb == kPastRun) ? 0 : eb;
+        if (j >= kStagesK && !mbar_wait(smem_addr(kempty + sk), ((j / kStagesK) - 1) & 1, abort_flag)) break;
+        uint32_t fb = smem_addr(kfull + sk);
+        mbar_arrive_expect_tx(fb, L::kKStage);
+        const uint32_t kdst = smem_addr(smem + L::kring + size_t(sk) * L::kKStage);
+        const int yk = (h * p.num_pages + (rank == 0 ? pa : pb)) * kPage;  // this CTA's K page
+#pragma unroll
+        for (int nb2 = 0; nb2 < NB; ++nb2) tma_load_2d(kdst + nb2 * kBoxBytes, &kmap, nb2 * kBoxCols, yk, fb);
+        if (j >= kStagesV && !mbar_wait(smem_addr(vempty + sv), ((j / kStagesV) - 1) & 1, abort_flag)) {
+          ++j;  // this step's K load was issued
+          break;
+        }
+        fb = smem_addr(vfull + sv);
+        mbar_arrive_expect_tx(fb, L::kVStage);
+        const uint32_t vdst = smem_addr(smem + L::vring + size_t(sv) * L::kVStage);
+        const int xv = static_cast<int>(rank) * kBoxCols;
+        tma_load_2d(vdst, &vmap, xv, (h * p.num_pages + pa) * kPage, fb);
+        tma_load_2d(vdst + kBoxBytes, &vmap, xv, (h * p.num_pages + pb) * kPage, fb);
+        ea = na;
+        eb = nb;
       }
       // do not leave while a copy may still land in this CTA's memory
-      const int issued = k;
-      for (int kk = max(0, issued - kStages); kk < issued; ++kk) {
-        const uint32_t fb = smem_addr(full_bar + kk % kStages);
+      const int issued = j;
+      for (int kk = max(0, issued - kStagesK); kk < issued; ++kk) {
+        const uint32_t fb = smem_addr(kfull + kk % kStagesK);
         const uint64_t t_0 = global_timer_ns();
-        while (!mbar_try_wait(fb, (kk / kStages) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+        while (!mbar_try_wait(fb, (kk / kStagesK) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
+        }
+      }
+      for (int kk = max(0, issued - kStagesV); kk < issued; ++kk) {
+        const uint32_t fb = smem_addr(vfull + kk % kStagesV);
+        const uint64_t t_0 = global_timer_ns();
+        while (!mbar_try_wait(fb, (kk / kStagesV) & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
         }
       }
     }
   } else if (warp == 1) {
-    // ================================ MMA =================================
-    if (lane == 0 && npages > 0) {
-      constexpr uint32_t kIdS = umma_idesc_bf16(kRows, 64, 0, 0);
-      constexpr uint32_t kIdPV = umma_idesc_bf16(kRows, L::kPvN, 0, 1);
-      // Descriptors of stage 0's K (K-major) and V (MN-major) boxes; another
+    if (rank != 0) {
+      // ============================ relay (rank 1) ==========================
+      if (lane == 0 && nsteps > 0) {
+        const uint32_t kfull0 = mapa_shared(smem_addr(kfull), 0);
+        const uint32_t vfull0 = mapa_shared(smem_addr(vfull), 0);
+        for (int j = 0; j < nsteps; ++j) {
+          const int sk = j % kStagesK, sv = j % kStagesV;
+          if (!mbar_wait(smem_addr(kfull + sk), (j / kStagesK) & 1, abort_flag)) break;
+          mbar_arrive_remote(kfull0 + sk * 8);
+          if (!mbar_wait(smem_addr(vfull + sv), (j / kStagesV) & 1, abort_flag)) break;
+          mbar_arrive_remote(vfull0 + sv * 8);
+        }
+      }
+    } else if (lane == 0 && nsteps > 0) {
+      // ======================= Q.K^T issuer (rank 0) ========================
+      constexpr uint32_t kIdS = umma_idesc_bf16(kTileRows, kStepKeys, 0, 0);
+      // Descriptors of stage 0's K tile and of the query rows (K-major); another
       // stage or K step adds its byte offset / 16 to the 14-bit address field,
       // which cannot carry (shared addresses stay below 256 KiB).
-      const uint32_t stage0 = smem_addr(smem + L::stages);
-      const uint64_t kdesc0 = umma_desc_sw128(stage0, 0, 1024);
-      const uint64_t vdesc0 = umma_desc_sw128(stage0 + NB * kBoxBytes, kBoxBytes, 1024);
-      // S_hf = Q_hf K^T for the page in stage s (Q from tensor memory)
-      auto issue_s = [&](int hf, int s) {
-        const uint64_t kd = kdesc0 + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
-        const uint32_t hc = tmem + hf * L::kHalfCols;
+      const uint64_t kdesc0 = umma_desc_sw128(smem_addr(smem + L::kring), 0, 1024);
+      const uint64_t qdesc0 = umma_desc_sw128(smem_addr(smem + L::qsm), 0, 1024);
+      // S_b = Q K^T of step j, once the softmax has read S_b of step j - 2
+      // (sfree is at most one phase past that: the softmax reads S_b of step
+      // j only after this product) and both CTAs' K pages have landed.
+      bool ok = mbar_wait(smem_addr(qfull), 0, abort_flag);
+      for (int j = 0; ok && j < nsteps; ++j) {
+        const int b = j & 1, sk = j % kStagesK;
+        ok = (j < 2 || mbar_wait(smem_addr(sfree + b), ((j - 2) >> 1) & 1, abort_flag)) &&
+             mbar_wait(smem_addr(kfull + sk), (j / kStagesK) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sc = tmem + L::kColS + static_cast<uint32_t>(b) * kStepKeys;
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>((sk * L::kKStage) >> 4);
 #pragma unroll
         for (int kk = 0; kk < DK; ++kk) {
-          const uint64_t bd = kd + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          umma_ts(hc + L::kColS, hc + L::kColQ + kk * 8, bd, kIdS, kk > 0);
+          const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          const uint32_t qoff = ((kk >> 2) * L::kQBox + (kk & 3) * 32) >> 4;
+          umma2_ss(sc, qdesc0 + qoff, kd + koff, kIdS, kk > 0);
         }
-        umma_commit(smem_addr(s_full + hf));
-      };
-      bool ok = mbar_wait(smem_addr(q_full), 0, abort_flag) && mbar_wait(smem_addr(full_bar), 0, abort_flag);
-      tc_fence_after();
-      if (ok) {
-#pragma unroll
-        for (int hf = 0; hf < kHalves; ++hf) issue_s(hf, 0);
+        umma2_commit_both(smem_addr(sfull + b));
+        umma2_commit_both(smem_addr(kempty + sk));
       }
-      int last_pv = -1;
-      for (int j = 0; ok && j < npages; ++j) {
-        const int s = j % kStages;
-        const uint64_t vd = vdesc0 + static_cast<uint64_t>((s * L::kStageBytes) >> 4);
+    }
+  } else if (warp == 10) {
+    if (rank == 0 && lane == 0 && nsteps > 0) {
+      // ========================= P.V issuer (rank 0) ========================
+      // One thread issues every P.V, in step order: O accumulates in order,
+      // and a finished P.V implies that every earlier one has finished.
+      constexpr uint32_t kIdPV = umma_idesc_bf16(kTileRows, L::kPvN, 0, 1);
+      const uint64_t vdesc0 = umma_desc_sw128(smem_addr(smem + L::vring), 0, 1024);
+      bool ok = true;
+      for (int j = 0; ok && j < nsteps; ++j) {
+        const int b = j & 1, sv = j % kStagesV;
+        ok = mbar_wait(smem_addr(pfull + b), (j >> 1) & 1, abort_flag) &&
+             mbar_wait(smem_addr(vfull + sv), (j / kStagesV) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t pc = tmem + L::kColP + static_cast<uint32_t>(b) * (kStepKeys / 2);
+        const uint64_t vd = vdesc0 + static_cast<uint64_t>((sv * L::kVStage) >> 4);
 #pragma unroll
-        for (int hf = 0; hf < kHalves && ok; ++hf) {
-          ok = mbar_wait(smem_addr(p_full + hf), j & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t hc = tmem + hf * L::kHalfCols;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // 64 keys, 16 per instruction
-            const uint64_t bd = vd + ((kk * 16 * 128) >> 4);
-            umma_ts(hc + L::kColO, hc + L::kColS + kk * 8, bd, kIdPV, (j > 0 || kk > 0));
-          }
-          umma_commit(smem_addr(pv_done + hf));
-          if (hf == kHalves - 1) {
-            umma_commit(smem_addr(empty_bar + s));
-            last_pv = j;
-          }
-          if (j + 1 < npages) {
-            const int s1 = (j + 1) % kStages;
-            if (hf == 0) {
-              ok = mbar_wait(smem_addr(full_bar + s1), ((j + 1) / kStages) & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            issue_s(hf, s1);
-          }
+        for (int kk = 0; kk < kStepKeys / 16; ++kk) {  // 16 keys per product
+          const uint64_t bd = vd + ((kk * 16 * 128) >> 4);
+          umma2_ts(tmem + L::kColO, pc + kk * 8, bd, kIdPV, (j > 0 || kk > 0));
         }
-      }
-      // the tensor memory is freed at the end: let the last products finish
-      if (last_pv >= 0) {
-        for (int hf = 0; hf < kHalves; ++hf) {
-          const uint32_t bar = smem_addr(pv_done + hf);
-          const uint64_t t_0 = global_timer_ns();
-          while (!mbar_try_wait(bar, last_pv & 1) && global_timer_ns() - t_0 < kWaitLimitNs) {
-          }
-        }
+        umma2_commit_both(smem_addr(vempty + sv));
+        umma2_commit_both(smem_addr(j + 1 < nsteps ? pvdone + b : odone));
       }
     }
   } else {
     // ============================== softmax ===============================
-    const int hf = (warp - 2) / 4;        // half of the tile
+    // Two groups of four warps take the steps in turn: group 0 (warps 2-5)
+    // the even steps, group 1 (warps 6-9) the odd ones, so that one group's
+    // loads and maxima overlap the other's exponentials.  Step j uses S_(j mod
+    // 2), so group g always reads and writes S_g.  Warps w and w + 4 share the
+    // tensor-memory lanes of quarter w % 4: thread r of each group owns query
+    // row r of this CTA.  The row's running max passes from the group of step
+    // j to the group of step j + 1 through shared memory (a named barrier that
+    // the publisher arrives on and the receiver waits on), together with the
+    // decision to go on, so a stop reaches both groups and neither waits for
+    // the other in vain.
+    const int grp = (warp - 2) >> 2;
     const int qt = warp & 3;              // tensor-memory lane quarter of this warp
-    const int row = hf * kRows + qt * 32 + lane;  // query row of the tile = token * G + head
+    const int rl = qt * 32 + lane;        // row of this CTA = tensor-memory lane
+    const int row = static_cast<int>(rank) * kRows + rl;  // row of the tile = token * G + head
     const int tl = row / G, g = row % G;
     const int lo = tok_lo[tl], hi = tok_hi[tl], run_id = tok_run[tl];
     const bool live = tl < nt && run_id >= 0;
-    const uint32_t hcol = tmem + (static_cast<uint32_t>(qt * 32) << 16) + hf * L::kHalfCols;
-    const int ctid = tid - 64;            // 0..255 among the softmax threads
+    const uint32_t lanes = static_cast<uint32_t>(qt * 32) << 16;
+    const int bar_pub = 1 + qt + 4 * grp;        // this group's hand-off to the other group
+    const int bar_sub = 1 + qt + 4 * (grp ^ 1);  // the other group's hand-off to this one
+    const int bar_fin = 9 + qt;                  // both groups, once at the end
+    float* hand_m = reinterpret_cast<float*>(smem + L::xchg);         // [2 step parities][128 rows]
+    int* hand_ok = reinterpret_cast<int*>(smem + L::xchg) + 2 * kRows;  // [2][128]
+    float* fin_m = reinterpret_cast<float*>(smem + L::xchg) + 4 * kRows;  // [2 groups][128]
+    float* fin_l = fin_m + 2 * kRows;
+    int* fin_ok = reinterpret_cast<int*>(fin_l + 2 * kRows);
     const size_t qrow = (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
-    // ---- this row's query into tensor memory (bf16 pairs, the A operand of Q.K) ----
-    if (npages > 0) {
+    const uint32_t pfull0 = mapa_shared(smem_addr(pfull), 0);
+    // ---- this row's query into shared memory (K-major, 128-byte swizzle: the
+    // A operand of Q.K^T), 16 bytes (eight head-dim columns) at a time ----
+    if (nsteps > 0 && grp == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow);
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {  // 8 bf16 pairs = two 16-byte loads per step
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (tl < nt) {
-          a = src[2 * c];
-          b = src[2 * c + 1];
-        }
-        const uint32_t r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        tmem_st8(hcol + L::kColQ + c * 8, r);
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 a = tl < nt ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + L::qsm + (c >> 3) * L::kQBox + swz128(rl, c & 7)) = a;
       }
-      tmem_st_wait();
-      tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(q_full));
+      // (the peer's tensor core reads these rows: publish at cluster scope)
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(qfull), 0));
     }
     // Every wait's outcome is made warp-uniform: the tensor-memory loads and
     // stores that follow are warp-collective.
-    float m_ref = -INFINITY, l_sum = 0.f;
-    uint32_t zero_uses = 0;
-    bool ok = true;
-    for (int j = 0; j < npages && ok; ++j) {
-      const int s = j % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(full_bar + s), (j / kStages) & 1, abort_flag));
-      if (!ok) break;
-      const PageInfo si = info[s];
-      const int kmin = run_kmin[si.run], kmax = run_kmax[si.run];
-      if (!si.valid || si.key_base < kmin || si.key_base + kPage > kmax) {
-        // Keys of this page outside the run's range may hold stale or
-        // uninitialised data: zero their value rows before P.V reads them.
-        uint8_t* vb = smem + L::stages + size_t(s) * L::kStageBytes + NB * kBoxBytes;
-        for (int i = ctid; i < kPage * NB * 8; i += kTileRows) {
-          const int key = i / (NB * 8), rest = i % (NB * 8);
-          if (!si.valid || si.key_base + key < kmin || si.key_base + key >= kmax)
-            *reinterpret_cast<uint4*>(vb + (rest >> 3) * kBoxBytes + key * 128 + (rest & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+    float m_ref = -INFINITY;   // the row's running max (log2 units) after this group's last step
+    float m_part = -INFINITY;  // reference of this group's partial sum
+    float l_part = 0.f;        // sum of this group's probabilities, relative to m_part
+    bool ok = true, stuck = false;
+    StepCursor cur;
+    int ea = kPastRun, eb = kPastRun;  // table entries of the step's two pages, read one step ahead
+    if (nsteps > 0) step_entries(p, run_row, run_first, run_kmax, misc[0], cur, ea, eb);
+    const uint32_t sc = tmem + lanes + L::kColS + static_cast<uint32_t>(grp) * kStepKeys;  // S_grp
+    const uint32_t pcol = tmem + lanes + L::kColP + static_cast<uint32_t>(grp) * (kStepKeys / 2);  // P_grp
+    const uint32_t sfree0 = mapa_shared(smem_addr(sfree), 0);
+    for (int j = 0; j < nsteps; ++j, cur.next(run_steps)) {
+      const int kmin = run_kmin[cur.run], kmax = run_kmax[cur.run];
+      const int lpa = run_first[cur.run] + 2 * cur.s;
+      const int kb = lpa * kPage;         // logical key of the step's first slot
+      // pages of the step that hold data: in the run and with a valid table entry
+      const bool va = ea >= 0 && ea < p.num_pages;
+      const bool vb = eb >= 0 && eb < p.num_pages;
+      {
+        StepCursor nc = cur;
+        nc.next(run_steps);
+        step_entries(p, run_row, run_first, run_kmax, misc[0], nc, ea, eb);
+      }
+      if ((j & 1) != grp) continue;
+      const int sv = j % kStagesV;
+      bool okw = !stuck && __all_sync(0xffffffffu, mbar_wait(smem_addr(sfull + grp), (j >> 1) & 1, abort_flag));
+      const bool partial = !(va && vb && kb >= kmin && kb + kStepKeys <= kmax);
+      if (okw && partial) {
+        // Keys of the step outside the run's range or on a missing page may
+        // hold stale or uninitialised data: zero their value rows (this CTA's
+        // columns) before P.V reads them.  Thread i of the group zeroes key row i.
+        okw = __all_sync(0xffffffffu, mbar_wait(smem_addr(vfull + sv), (j / kStagesV) & 1, abort_flag));
+        const int key = rl;
+        const bool vpage = key < kPage ? va : vb;
+        if (okw && (!vpage || kb + key < kmin || kb + key >= kmax)) {
+          uint8_t* vrow = smem + L::vring + size_t(sv) * L::kVStage + (key >> 6) * kBoxBytes + (key & 63) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
-        mbar_arrive(smem_addr(zero_bar));
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(zero_bar), zero_uses & 1u, abort_flag));
-        ++zero_uses;
       }
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(s_full + hf), j & 1, abort_flag));
-      if (!ok) break;
       tc_fence_after();
-      float x[64];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(hcol + L::kColS, r0);
-        tmem_ld32(hcol + L::kColS + 32, r1);
+      float x[kStepKeys];
+      if (okw) {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(sc, r0);
+        tmem_ld32(sc + 32, r1);
+        tmem_ld32(sc + 64, r2);
+        tmem_ld32(sc + 96, r3);
         tmem_ld_wait();
+        // S_grp may take the next scores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(sfree0 + grp * 8);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           x[i] = __uint_as_float(r0[i]);
           x[32 + i] = __uint_as_float(r1[i]);
+          x[64 + i] = __uint_as_float(r2[i]);
+          x[96 + i] = __uint_as_float(r3[i]);
         }
-      }
-      // visible keys of this page for this row: [ka, ke)
-      const bool in_run = live && si.valid && si.run == run_id;
-      const int ka = in_run ? max(lo - si.key_base, 0) : kPage;
-      const int ke = in_run ? max(ka, min(hi - si.key_base, kPage)) : kPage;
-      if (!__all_sync(0xffffffffu, ka == 0 && ke == kPage)) {
+      } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = (i >= ka && i < ke) ? x[i] : -INFINITY;
+        for (int i = 0; i < kStepKeys; ++i) x[i] = -INFINITY;
       }
-      // row max as a tree of independent maxima
+      // visible keys of this step for this row: [a0, e0), minus a missing page
+      const bool in_run = live && cur.run == run_id;
+      const int ka = in_run ? max(lo - kb, 0) : kStepKeys;
+      const int ke = in_run ? max(ka, min(hi - kb, kStepKeys)) : kStepKeys;
+      const int ma = va ? 0 : kPage, me = vb ? kStepKeys : kPage;  // keys on valid pages: [ma, me)
+      const int a0 = max(ka, ma), e0 = min(ke, me);
+      if (!__all_sync(0xffffffffu, a0 == 0 && e0 == kStepKeys)) {
+#pragma unroll
+        for (int i = 0; i < kStepKeys; ++i) x[i] = (i >= a0 && i < e0) ? x[i] : -INFINITY;
+      }
+      // row max as a tree of independent three-input maxima
       float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(x[i], x[i + 8]);
+      for (int k = 0; k < 8; ++k) {
+        m8[k] = fmax3(x[k], x[8 + k], x[16 + k]);
 #pragma unroll
-      for (int i = 16; i < 64; i += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], x[i + k]);
-      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int i = 24; i < kStepKeys - 8; i += 16) m8[k] = fmax3(m8[k], x[i + k], x[i + 8 + k]);
+        m8[k] = fmaxf(m8[k], x[kStepKeys - 8 + k]);
+      }
+      const float mraw = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;  // log2 units
-      // running max: rescale O only when it grows by more than 2^8
-      float alpha = 1.f;
+      // the row's running max before this step, from the group of step j - 1
+      if (j > 0) {
+        named_barrier_sync(bar_sub, 64);
+        m_ref = hand_m[((j - 1) & 1) * kRows + rl];
+        okw = okw && hand_ok[((j - 1) & 1) * kRows + rl] != 0;
+      }
+      ok = __all_sync(0xffffffffu, okw);
+      // new running max: it moves only when this step's max exceeds it by
+      // more than 2^8, and then O is rescaled
+      float m_new = m_ref, alpha = 1.f;
       if (mx != -INFINITY) {
         if (m_ref == -INFINITY) {
-          m_ref = mx;
+          m_new = mx;
         } else if (mx > m_ref + kRescaleLog2) {
+          m_new = mx;
           alpha = exp2f(m_ref - mx);
-          m_ref = mx;
-          l_sum *= alpha;
         }
       }
+      // hand it on before the exponentials, so the other group can go on
+      if (j + 1 < nsteps) {
+        hand_m[(j & 1) * kRows + rl] = m_new;
+        hand_ok[(j & 1) * kRows + rl] = ok ? 1 : 0;
+        __syncwarp();
+        named_barrier_arrive(bar_pub, 64);
+      }
+      if (!ok) break;
+      m_ref = m_new;
+      // this group's partial sum follows the row's reference
+      if (m_part != m_ref) {
+        if (m_part != -INFINITY) l_part *= exp2f(m_part - m_ref);
+        m_part = m_ref;
+      }
+      // probabilities 2^(s * scale * log2(e) - m_ref), packed to bf16 over
+      // the first 64 columns of S_grp (paired fp32: one fma and one add per
+      // two keys)
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+      const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2), n2 = f32x2(nbase, nbase);
+      // P_grp is free once P.V of step j - 2 has read it.  (This group waited
+      // for P.V of step j - 4 before it wrote P at step j - 2, so pvdone[grp]
+      // is at most one phase behind step j - 2 here, never two.)
+      if (j >= 2) stuck = stuck || !__all_sync(0xffffffffu, mbar_wait(smem_addr(pvdone + grp), ((j - 2) >> 1) & 1, abort_flag));
+      tc_fence_after();
+      uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};  // running sums, two keys per register
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a0v, a1v;
+          f32x2_split(fma_f32x2(f32x2(x[hh * 32 + 2 * i], x[hh * 32 + 2 * i + 1]), c2, n2), a0v, a1v);
+          const float e0v = ex2_approx(a0v), e1v = ex2_approx(a1v);
+          s2[i & 3] = add_f32x2(s2[i & 3], f32x2(e0v, e1v));
+          pk[i] = pack_bf16x2(e0v, e1v);
+        }
+        tmem_st16(pcol + hh * 16, pk);
+      }
       if (__any_sync(0xffffffffu, alpha != 1.f) && j >= 1) {
-        // P.V of page j - 1
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(pv_done + hf), (j - 1) & 1, abort_flag));
-        if (!ok) break;
+        // the running max grew: rescale this row of O once P.V of step j - 1
+        // (written by the other group) has finished, before P.V of step j.
+        // (P.V runs in step order and the wait above saw step j - 2 finish,
+        // so step j - 3 has finished too: that barrier is at most one phase
+        // behind step j - 1.)
+        // (this group's hand-off for step j + 1 has gone out already: if the
+        // wait gives up, the failure travels with its next hand-off instead)
+        stuck = stuck || !__all_sync(0xffffffffu, mbar_wait(smem_addr(pvdone + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
+                                                             abort_flag));
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < L::kPvN / 32; ++c) {
+        for (int c = 0; c < (stuck ? 0 : L::kPvN / 32); ++c) {
           uint32_t r[32];
-          tmem_ld32(hcol + L::kColO + c * 32, r);
+          tmem_ld32(tmem + lanes + L::kColO + c * 32, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(hcol + L::kColO + c * 32, r);
+          tmem_st32(tmem + lanes + L::kColO + c * 32, r);
         }
-        tmem_st_wait();
       }
-      // probabilities 2^(s * scale * log2(e) - m_ref), packed to bf16
-      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[32];
-      float r8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) r8[k] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float e0 = ex2_approx(__fmaf_rn(x[2 * i], p.scale_log2, nbase));
-        const float e1 = ex2_approx(__fmaf_rn(x[2 * i + 1], p.scale_log2, nbase));
-        r8[i & 7] += e0 + e1;
-        pk[i] = pack_bf16x2(e0, e1);
-      }
-      l_sum += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-      tmem_st32(hcol + L::kColS, pk);  // P over the scores just read
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_full + hf));
+      if (lane == 0) {
+        if (partial) mbar_arrive_cluster(pfull0 + grp * 8);  // publishes the zeroed value rows
+        else mbar_arrive_remote(pfull0 + grp * 8);
+      }
+      {
+        float u0, u1;
+        f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), u0, u1);
+        l_part += u0 + u1;
+      }
     }
-    // ---- normalise and store this row ----
-    if (ok && npages > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(pv_done + hf), (npages - 1) & 1, abort_flag));
+    // ---- normalise and store this row: group g stores half g of head_dim ----
+    // (the last P.V commits to a barrier of its own: here pvdone may be one
+    // phase short of it or already past it, which a parity wait cannot tell)
+    if (nsteps > 0) {
+      const bool okw = ok && !stuck && __all_sync(0xffffffffu, mbar_wait(smem_addr(odone), 0, abort_flag));
       tc_fence_after();
+      fin_m[grp * kRows + rl] = m_part;
+      fin_l[grp * kRows + rl] = l_part;
+      fin_ok[grp * kRows + rl] = okw ? 1 : 0;
+      named_barrier_sync(bar_fin, 64);
+      const float mo = fin_m[(grp ^ 1) * kRows + rl], lo_ = fin_l[(grp ^ 1) * kRows + rl];
+      ok = __all_sync(0xffffffffu, okw && fin_ok[(grp ^ 1) * kRows + rl] != 0);
+      // both partial sums relative to the final reference (the larger one)
+      const float mf = fmaxf(m_part, mo);
+      const float la = m_part == -INFINITY ? 0.f : l_part * exp2f(m_part - mf);
+      const float lb = mo == -INFINITY ? 0.f : lo_ * exp2f(mo - mf);
+      l_part = grp == 0 ? la + lb : lb + la;
     }
-    uint16_t* dst = p.out + qrow;
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    uint16_t* dst = p.out + qrow + grp * (D / 2);
+    const float inv = l_part > 0.f ? 1.f / l_part : 0.f;
 #pragma unroll 1
-    for (int c = 0; c < L::kPvN / 16; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t r[16];
-      if (ok && npages > 0) {
-        tmem_ld16(hcol + L::kColO + c * 16, r);
+      if (ok && nsteps > 0) {
+        tmem_ld16(tmem + lanes + L::kColO + grp * (D / 2) + c * 16, r);
         tmem_ld_wait();
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = 0u;
       }
-      if (tl < nt && c * 16 < D) {
+      if (tl < nt) {
         uint2* o = reinterpret_cast<uint2*>(dst + c * 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float a0 = live ? __uint_as_float(r[4 * i]) * inv : 0.f;
-          const float a1 = live ? __uint_as_float(r[4 * i + 1]) * inv : 0.f;
-          const float a2 = live ? __uint_as_float(r[4 * i + 2]) * inv : 0.f;
-          const float a3 = live ? __uint_as_float(r[4 * i + 3]) * inv : 0.f;
-          o[i] = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+          const float a0v = live ? __uint_as_float(r[4 * i]) * inv : 0.f;
+          const float a1v = live ? __uint_as_float(r[4 * i + 1]) * inv : 0.f;
+          const float a2v = live ? __uint_as_float(r[4 * i + 2]) * inv : 0.f;
+          const float a3v = live ? __uint_as_float(r[4 * i + 3]) * inv : 0.f;
+          o[i] = make_uint2(pack_bf16x2(a0v, a1v), pack_bf16x2(a2v, a3v));
         }
       }
     }
   }
   if (*abort_flag && lane == 0 && p.status != nullptr) atomicOr(p.status, LNK_DEV_TIMEOUT);
+  // neither CTA frees its tensor memory or leaves while the pair's products,
+  // copies or remote arrivals may still touch it
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+  if (warp == 1) tmem2_dealloc(tmem, L::kTmemCols);
 }
 
 template <int D>
@@ -515,8 +671,9 @@ cudaError_t launch_chunk_t(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   const int bytes = static_cast<int>(TcSmem<D>::bytes);
   cudaError_t err = set_max_dynamic_smem(reinterpret_cast<const void*>(chunk_kernel<D>), bytes);
   if (err != cudaSuccess) return err;
-  dim3 grid(p.num_tiles, p.hkv);
-  chunk_kernel<D><<<grid, kThreads, bytes, stream>>>(kmap, vmap, p);
+  const long long grid = 2ll * p.num_tiles * p.hkv;  // a cluster of two CTAs per (tile, kv head)
+  if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+  chunk_kernel<D><<<static_cast<unsigned>(grid), kThreads, bytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
