@@ -105,7 +105,11 @@ typedef struct lnk_attn_desc {
  *   input) and the division is one IEEE float32 division, saturating to
  *   +-448.  Attention uses the dequantized values e4m3(c) * scale.  Chunk
  *   attention (P > 0 in lnk_paged_step_attn) is supported on bf16 pools only;
- *   decode rows are supported on both. */
+ *   decode rows are supported on both.  Decode over 8-bit pools converts the
+ *   rotated queries to f16 (exactly, for magnitudes in [2^-14, 65504]): a
+ *   query element above 65504 in magnitude becomes infinite there, and one
+ *   below 2^-14 loses precision or becomes zero, so the queries must stay
+ *   within that range (unit-scale projections do by far). */
 #define LNK_KV_BF16 0
 #define LNK_KV_E4M3 1
 
@@ -197,6 +201,14 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  *             (256-byte aligned; zero-filled before its first use, and again
  *             after a call that reported LNK_DEV_TIMEOUT; the kernel leaves
  *             its counters at zero otherwise)
+ *
+ * Ordering with the preceding kernel: the decode kernel is launched as a
+ * programmatic dependent launch and reads `positions` (and only that) before
+ * it waits for the kernel before it on the stream; q, the table and the pools
+ * are read after the wait.  So `positions` must not be written by the kernel
+ * immediately preceding this call on the same stream (lnk_paged_append_rope
+ * only reads it); a caller that computes positions on the device should
+ * write them earlier, or put another operation in between.
  */
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
                                  const int32_t* positions, const int32_t* table,
