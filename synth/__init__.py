@@ -144,6 +144,18 @@ def e4m3_codes(key: int, start: int, count: int) -> np.ndarray:
     return ((sign << np.uint64(7)) | (e << np.uint64(3)) | m).astype(np.uint8)
 
 
+# every finite E4M3 code (all but the two NaN codes, S.1111.111)
+E4M3_FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def e4m3_codes_all(key: int, start: int, count: int) -> np.ndarray:
+    """Bytes for a prefilled 8-bit pool drawn from every finite E4M3 code
+    (subnormals, zeros and the saturated +-448 included): byte i is finite code
+    number (SplitMix64 output i) mod 254 (host only)."""
+    h = splitmix64(key, start, count)
+    return E4M3_FINITE[(h % np.uint64(len(E4M3_FINITE))).astype(np.int64)]
+
+
 def tensor_bf16(seed: int, stream: int, shape) -> np.ndarray:
     n = int(np.prod(shape)) if len(shape) else 1
     return normal_bf16(stream_key(seed, stream), 0, n).reshape(shape)
@@ -195,6 +207,7 @@ class Workload:
     q_scale: float = 1.0        # power of two multiplying the step's queries
     k_page_scale: Optional[dict] = None  # physical page -> power of two multiplying its K values
     gamma_halves: Optional[tuple] = None  # QK-norm gamma (a, b): a on the first half of D, b on the second
+    e4m3_all: bool = False      # 8-bit pools drawn from every finite code (host only)
 
     @property
     def B(self) -> int:
@@ -231,7 +244,7 @@ class Workload:
     def device_fillable(self) -> bool:
         """The pool can be filled on the device (``synth/fill.cu``): Irwin-Hall
         values with no page scaling."""
-        return self.dist == "ih" and not self.k_page_scale
+        return self.dist == "ih" and not self.k_page_scale and not self.e4m3_all
 
     def _values(self, key: int, start: int, count: int) -> np.ndarray:
         if self.dist == "gauss":
@@ -280,10 +293,13 @@ class Workload:
                 out[:, sl] = scale_bf16_pow2(out[:, sl], f)
         return out
 
+    def _codes(self, key: int, start: int, count: int) -> np.ndarray:
+        return (e4m3_codes_all if self.e4m3_all else e4m3_codes)(key, start, count)
+
     def pool_e4m3(self, which: str) -> np.ndarray:
         """The whole 8-bit pool [Hkv][num_pages * 64][D] of codes (prefilled context)."""
         n = self.hkv * self.pool_positions * self.head_dim
-        return e4m3_codes(self.pool_key(which), 0, n).reshape(self.hkv, self.pool_positions, self.head_dim)
+        return self._codes(self.pool_key(which), 0, n).reshape(self.hkv, self.pool_positions, self.head_dim)
 
     def pool_pages_e4m3(self, which: str, kv_head: int, pages: np.ndarray) -> np.ndarray:
         """Codes of the listed pages of one kv head, [len(pages)][64][D]."""
@@ -291,7 +307,7 @@ class Workload:
         out = np.empty((len(pages), PAGE_SIZE, self.head_dim), dtype=np.uint8)
         for i, pg in enumerate(np.asarray(pages).tolist()):
             start = kv_head * per_head + int(pg) * PAGE_SIZE * self.head_dim
-            out[i] = e4m3_codes(self.pool_key(which), start, PAGE_SIZE * self.head_dim).reshape(PAGE_SIZE, self.head_dim)
+            out[i] = self._codes(self.pool_key(which), start, PAGE_SIZE * self.head_dim).reshape(PAGE_SIZE, self.head_dim)
         return out
 
     def pool_pages(self, which: str, kv_head: int, pages: np.ndarray) -> np.ndarray:

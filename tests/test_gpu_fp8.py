@@ -41,7 +41,7 @@ def _u8(t):
 class F8Step:
     """Device buffers of one workload step over 8-bit pools."""
 
-    def __init__(self, w, fill="host"):
+    def __init__(self, w, fill="host", k_scale=K_SCALE, v_scale=V_SCALE):
         import paged_kv_gqa_row_gb300 as lnk
         self.w, self.lnk = w, lnk
         shape = (w.hkv, w.pool_positions, w.head_dim)
@@ -62,7 +62,7 @@ class F8Step:
         self.out = torch.zeros_like(self.q_out)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.desc = lnk.attn_desc(w.hq, w.hkv, w.head_dim, w.num_pages, w.num_rows, w.pages_per_row,
-                                  window=w.window, kv_dtype=lnk.KV_E4M3, k_scale=K_SCALE, v_scale=V_SCALE)
+                                  window=w.window, kv_dtype=lnk.KV_E4M3, k_scale=k_scale, v_scale=v_scale)
         self.rope = lnk.rope_desc(w.theta, w.llama3)
         self.ws_bytes = max(lnk.lnk_paged_workspace_size(self.desc, max(w.B, 1)), 256)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
@@ -80,23 +80,23 @@ class F8Step:
                                        self.v_pool, self.out[w.P:], w.B, self.ws, self.ws_bytes, self.status)
 
 
-def _oracle_full(w):
+def _oracle_full(w, k_scale=K_SCALE, v_scale=V_SCALE):
     inv = orope.inv_freq(w.theta, w.head_dim, w.llama3)
     q_out, kc, vc = ofp8.append_rope(w.step_q(), w.step_k(), w.step_v(), w.token_positions(), w.token_rows(),
-                                     w.table, w.pool_e4m3("k"), w.pool_e4m3("v"), inv, K_SCALE, V_SCALE,
+                                     w.table, w.pool_e4m3("k"), w.pool_e4m3("v"), inv, k_scale, v_scale,
                                      gamma_q=w.gamma_q(), gamma_k=w.gamma_k(), eps=w.norm_eps)
-    out = ofp8.decode_attention(q_out[w.P:], w.dec_positions, w.table, kc, vc, K_SCALE, V_SCALE, w.window)
+    out = ofp8.decode_attention(q_out[w.P:], w.dec_positions, w.table, kc, vc, k_scale, v_scale, w.window)
     return q_out, kc, vc, out
 
 
-def _check_full(w, poison=False):
-    dev = F8Step(w)
+def _check_full(w, poison=False, k_scale=K_SCALE, v_scale=V_SCALE):
+    dev = F8Step(w, k_scale=k_scale, v_scale=v_scale)
     if poison:
         _poison(w, dev)
     dev.append()
     dev.decode()
     torch.cuda.synchronize()
-    q_want, kc, vc, out_want = _oracle_full(w)
+    q_want, kc, vc, out_want = _oracle_full(w, k_scale, v_scale)
     assert_ulp_close(to_bits(dev.q_out), q_want, "q_out")
     kg, vg = _u8(dev.k_pool), _u8(dev.v_pool)
     if poison:  # the oracle's pool has finite codes where the device pool was poisoned
@@ -148,6 +148,20 @@ def test_e4m3_append_and_decode_match_oracle(case):
 def test_e4m3_decode_ignores_nan_codes_in_unread_slots():
     w = synth.custom(seed=77, hq=8, hkv=2, head_dim=128, dec_lengths=[5, 64, 130, 300])
     _check_full(w, poison=True)
+
+
+@pytest.mark.parametrize("hq,hkv,d,window", [(8, 2, 128, 0), (6, 6, 96, 100), (16, 2, 64, 0)],
+                         ids=["gqa4-128", "mha96-window100", "gqa8-64"])
+def test_e4m3_every_finite_code_in_the_pools(hq, hkv, d, window):
+    """Prefilled pools drawn from all 254 finite codes: subnormals, zeros, the
+    smallest and the saturated +-448 are all read by the decode kernel.  Small
+    pool scales (K x 2^-6, V x 2^-7) keep the outputs at unit scale."""
+    w = synth.custom(seed=zlib.crc32(f"e4m3-all-{hq}-{d}".encode()) % 10000, hq=hq, hkv=hkv, head_dim=d,
+                     dec_lengths=[1, 64, 65, 700, 2000, 3000], window=window)
+    w.e4m3_all = True
+    codes = w.pool_e4m3("k")
+    assert len(np.unique(codes)) == 254  # every finite code occurs
+    _check_full(w, k_scale=2.0 ** -6, v_scale=2.0 ** -7)
 
 
 @pytest.mark.parametrize("name, scale, rows", [("mistral", 0.06, 12), ("qwen3", 0.05, 40), ("phi3_window", 0.6, 8)])
