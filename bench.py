@@ -386,7 +386,11 @@ class GpuWorkload:
         self.stream = torch.cuda.Stream(device=dev)
         self.s_handle = self.stream.cuda_stream
         self.inputs = (self.q, self.k, self.v, self.pos, self.table)
-        self.launches_per_step = 1 + (1 if w.P else 0) + (1 if w.B else 0)
+        if w.P == 0:  # lnk_paged_decode_step: one kernel or two
+            self.launches_per_step = lnk.lnk_paged_decode_step_launches(self.desc, w.B)
+        else:
+            self.launches_per_step = 1 + 1 + (1 if w.B else 0)
+        self.one_kernel = w.P == 0 and self.launches_per_step == 1
 
     def attend(self, kp, vp, q_src, out_dst, tab):
         w, lnk = self.w, self.lnk
@@ -410,9 +414,19 @@ class GpuWorkload:
                                     kp, vp, self.out, None, None, w.P, 0, 0, None, 0, self.status, self.s_handle)
 
     def step(self, i, inp, ev=None, out_dst=None):
+        """One whole step.  Decode-only steps are one lnk_paged_decode_step call
+        (append and attention, one kernel for small launches); steps with prompt
+        chunks are lnk_paged_append_rope then lnk_paged_step_attn.  With `ev`,
+        events around the attention call (two calls then, for decode-only steps:
+        the append and lnk_paged_decode_attn)."""
         w = self.w
         qq, kk, vv, pp, tab = inp
         kp, vp = self.pools[i % self.copies]
+        if w.P == 0 and ev is None:
+            self.lnk.lnk_paged_decode_step(self.desc, self.rd, qq, kk, vv, pp, tab, self.gq, self.gk, w.norm_eps,
+                                           kp, vp, self.q_out, self.out if out_dst is None else out_dst, w.B,
+                                           self.ws, self.ws_bytes, self.status, self.s_handle)
+            return
         self.lnk.lnk_paged_append_rope(self.desc, self.rd, qq, kk, vv, pp, self.rows, None, tab, self.gq, self.gk,
                                        w.norm_eps, kp, vp, self.q_out, w.T, self.status, self.s_handle)
         if ev is not None:
@@ -454,32 +468,44 @@ class GpuWorkload:
             dist.barrier()
         return t_start.elapsed_time(t_end)
 
-    def kernel_times(self, n):
-        """Average device time of the attention call and, for steps with both
-        prompt chunks and decode rows, of each of its two kernels alone: events
-        on the launching stream around the call, over n steps of the same
-        workload.  (Events between the append and the attention call would stop
-        the attention kernel from overlapping the append kernel's tail, so the
+    def kernel_times(self, n, step_ms=None):
+        """Average device time of the step's kernels, timed on the launching
+        stream with CUDA events around each call, over n calls on the same
+        workload: the attention call ("attn"; for decode-only steps
+        lnk_paged_decode_attn alone, call after call) and, for steps with both
+        prompt chunks and decode rows, each of its two kernels alone.  A
+        decode step that is one kernel (lnk_paged_decode_step's one-kernel
+        form) is that kernel: its time is the timed region's time per step
+        (step_ms), since events around calls that short would time the host.
+        (Events between the append and the attention call would stop the
+        attention kernel from overlapping the append kernel's tail, so the
         whole-step timing has none.)"""
         torch, w = self.torch, self.w
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        with torch.cuda.stream(self.stream):
-            for i in range(n):
-                self.step(i, self.inputs, ev[i])
-        self.stream.synchronize()
-        times = {"attn": sum(a.elapsed_time(b) for a, b in ev) / n}
-        if w.P and w.B:
-            for part in ("decode", "chunk"):
-                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                      for _ in range(n)]
-                with torch.cuda.stream(self.stream):
-                    for i in range(n):
-                        kp, vp = self.pools[i % self.copies]
-                        ev[i][0].record(self.stream)
-                        self.attend_part(kp, vp, part)
-                        ev[i][1].record(self.stream)
-                self.stream.synchronize()
-                times[part] = sum(a.elapsed_time(b) for a, b in ev) / n
+
+        def timed_calls(call):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            with torch.cuda.stream(self.stream):
+                for i in range(n):
+                    ev[i][0].record(self.stream)
+                    call(i)
+                    ev[i][1].record(self.stream)
+            self.stream.synchronize()
+            return sum(a.elapsed_time(b) for a, b in ev) / n
+
+        if self.one_kernel:
+            times = {"attn": step_ms}
+        elif w.P == 0:
+            times = {"attn": timed_calls(lambda i: self.attend_part(*self.pools[i % self.copies], "decode"))}
+        else:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            with torch.cuda.stream(self.stream):
+                for i in range(n):
+                    self.step(i, self.inputs, ev[i])
+            self.stream.synchronize()
+            times = {"attn": sum(a.elapsed_time(b) for a, b in ev) / n}
+            if w.B:
+                for part in ("decode", "chunk"):
+                    times[part] = timed_calls(lambda i: self.attend_part(*self.pools[i % self.copies], part))
         self.check_status()
         return times
 
@@ -491,13 +517,18 @@ class GpuWorkload:
         w, parts = self.w, self.parts
         peak, peak_kind = read_peaks()
         tpeak, tkind = read_tensor_peak()
-        timing = (f"CUDA events around the call on its stream, average over {kt_steps} steps of the same "
+        timing = (f"CUDA events around the call on its stream, average over {kt_steps} calls on the same "
                   "workload right after the timed region")
+        if self.one_kernel:
+            timing = "the timed region's device time per step (the step is this one kernel)"
         if w.B:
             dec_ms = times["decode"] if w.P else times["attn"]
-            dec_bytes = parts["decode_call"]
+            # (a one-kernel decode step: the kernel also reads the step's q/k/v and writes k/v and q_out)
+            dec_bytes = parts["step"] if self.one_kernel else parts["decode_call"]
             achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-            r = {"bound": "hbm", "kernel": "decode_kernel (lnk_paged_decode_attn over the step's decode rows)",
+            name = ("decode_kernel (lnk_paged_decode_step in one kernel: append and attention)" if self.one_kernel
+                    else "decode_kernel (lnk_paged_decode_attn over the step's decode rows)")
+            r = {"bound": "hbm", "kernel": name,
                  "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                  "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                  "traffic": recorded_traffic("decode.cu", config + ("_e4m3" if self.e4m3 else "")),
@@ -629,7 +660,7 @@ def run_gpu(args, rank, world, dist):
         time.sleep(0.3)
     elapsed_ms = g.timed(args.steps, dist, sampler)
     kt_steps = max(1, min(args.steps, 500))
-    times = g.kernel_times(kt_steps)
+    times = g.kernel_times(kt_steps, elapsed_ms / args.steps)
     clocks = sampler.stop() if sampler else None
     e2e_steps = max(1, min(args.steps, 200))
     e2e_ms, h2d, d2h, e2e_how = g.e2e(e2e_steps, elapsed_ms / args.steps, dist)

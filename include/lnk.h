@@ -8,6 +8,8 @@
  *                           its slot of the shared page pool;
  *   lnk_paged_decode_attn   one query token per decode row over that row's pages
  *                           (the serving step "decode_paged");
+ *   lnk_paged_decode_step   append_rope then decode_attn for one token per
+ *                           decode row (one kernel for small launches);
  *   lnk_paged_step_attn     packed prompt chunks plus decode rows in one call
  *                           ("step_paged"; with no decode rows it is
  *                           "prefill_paged").
@@ -172,6 +174,14 @@ size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows);
  * angles of 2^20 and more and for the QK-norm factor) and rounded once to
  * bf16 (nearest even); v is copied bit for bit.  Two tokens writing one slot
  * race (the engine's padding tokens write a shared dump slot nobody reads).
+ *
+ * Ordering with the preceding kernel: the append kernel is launched as a
+ * programmatic dependent launch and reads `positions`, `rows`, `slots` and
+ * `table` (and only those) before it waits for the kernel before it on the
+ * stream; q, k, v, the QK-norm weights, the pools and q_out are touched after
+ * the wait.  So those four must not be written by the kernel immediately
+ * preceding this call on the same stream (this library's kernels only read
+ * them).
  */
 lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope,
                                  const lnk_bf16* q, const lnk_bf16* k, const lnk_bf16* v,
@@ -203,18 +213,61 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  *             its counters at zero otherwise)
  *
  * Ordering with the preceding kernel: the decode kernel is launched as a
- * programmatic dependent launch and reads `positions` (and only that) before
- * it waits for the kernel before it on the stream; q, the table and the pools
- * are read after the wait.  So `positions` must not be written by the kernel
- * immediately preceding this call on the same stream (lnk_paged_append_rope
- * only reads it); a caller that computes positions on the device should
- * write them earlier, or put another operation in between.
+ * programmatic dependent launch and reads `positions` and `table` (and only
+ * those) before it waits for the kernel before it on the stream; q, the pools
+ * and the workspace are touched after the wait.  So `positions` and `table`
+ * must not be written by the kernel immediately preceding this call on the
+ * same stream (lnk_paged_append_rope only reads them); a caller that computes
+ * them on the device should write them earlier, or put another operation in
+ * between.  The decode kernel in turn lets the next kernel on the stream start
+ * early (programmatic dependent launch): a kernel launched that way must wait
+ * for it (griddepcontrol.wait) before reading `out` or writing what it reads.
  */
 lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped,
                                  const int32_t* positions, const int32_t* table,
                                  const lnk_bf16* k_pool, const lnk_bf16* v_pool,
                                  lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes,
                                  int32_t* dev_status, lnk_stream stream);
+
+/*
+ * lnk_paged_decode_step -- a whole decode step: append, then attention.
+ *
+ * Defines: "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
+ * (decode_rows: write the row's new token at its position, then attend over
+ * the row up to it); "Mistral 7B Instruct v0.3", Entries table (decode_paged).
+ *
+ * The same results as lnk_paged_append_rope(desc, rope, q, k, v, positions,
+ * rows = NULL, slots = NULL, table, q_norm_w, k_norm_w, norm_eps, k_pool,
+ * v_pool, q_out, T = B, ...) followed by lnk_paged_decode_attn(desc, q_out,
+ * positions, table, k_pool, v_pool, out, B, ...), bit for bit: decode row b's
+ * token is token b, written through table row b.  Arguments are those two
+ * calls' (q_out must be 16-byte aligned); every check of both is made before
+ * anything is enqueued.
+ *
+ * When B * num_kv_heads is at most the decode grid (one CTA per SM, two for
+ * 8-bit pools when they fit) and at least half the SM count, and a (row, kv
+ * head) pair can span at most 16 pages (pages_per_row, or the window's
+ * pages), it is one kernel: the
+ * CTA that attends for pair (b, h) first rotates that pair's query heads and
+ * key head and writes its k/v row into the pool, then loads the row's pages
+ * (the last one after that write).  Otherwise it is the two kernels above.
+ * In the one-kernel form a token's pool slot must not be visible to another
+ * decode row of the same call (rows share only pages below their positions,
+ * as copy on write keeps them), and `positions` and `table` must not be
+ * written by the kernel immediately preceding the call on the stream.
+ */
+lnk_status lnk_paged_decode_step(const lnk_attn_desc* desc, const lnk_rope_desc* rope,
+                                 const lnk_bf16* q, const lnk_bf16* k, const lnk_bf16* v,
+                                 const int32_t* positions, const int32_t* table,
+                                 const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w,
+                                 float norm_eps, lnk_bf16* k_pool, lnk_bf16* v_pool,
+                                 lnk_bf16* q_out, lnk_bf16* out, int32_t B, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_status, lnk_stream stream);
+
+/* Kernels that lnk_paged_decode_step enqueues for B rows on the current
+ * device: 1 (the one-kernel form) or 2; 0 for B = 0; -1 for a descriptor or
+ * B that the call would reject. */
+int32_t lnk_paged_decode_step_launches(const lnk_attn_desc* desc, int32_t B);
 
 /*
  * lnk_paged_step_attn -- packed prompt chunks and decode rows in one call.

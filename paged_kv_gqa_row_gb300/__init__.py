@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     lnk_paged_append_rope,
     lnk_paged_copy_pages,
     lnk_paged_decode_attn,
+    lnk_paged_decode_step,
+    lnk_paged_decode_step_launches,
     lnk_paged_decode_attn_static,
     lnk_paged_step_attn,
     lnk_paged_workspace_size,

@@ -28,7 +28,8 @@ DEV_BAD_ROW, DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_BAD_SLOT = 0x01, 0x02, 0x04, 0x
 DEV_SEGMENT, DEV_BAD_LAST, DEV_TIMEOUT = 0x10, 0x20, 0x40
 
 EXPORTED = ["lnk_status_string", "lnk_rope_inv_freq", "lnk_paged_workspace_size",
-            "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_step_attn",
+            "lnk_paged_append_rope", "lnk_paged_decode_attn", "lnk_paged_decode_step",
+            "lnk_paged_decode_step_launches", "lnk_paged_step_attn",
             "lnk_paged_decode_attn_static", "lnk_pager_create", "lnk_pager_destroy", "lnk_pager_reserve",
             "lnk_pager_fork", "lnk_pager_prepare_append", "lnk_pager_release", "lnk_pager_table",
             "lnk_pager_free_pages", "lnk_pager_refcount", "lnk_paged_copy_pages",
@@ -71,6 +72,12 @@ _lib.lnk_paged_append_rope.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(
 _lib.lnk_paged_decode_attn.restype = ctypes.c_int
 _lib.lnk_paged_decode_attn.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                        c_i32, c_vp, c_size, c_vp, c_vp]
+_lib.lnk_paged_decode_step.restype = ctypes.c_int
+_lib.lnk_paged_decode_step.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(RopeDesc),
+                                       c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_f32,
+                                       c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_size, c_vp, c_vp]
+_lib.lnk_paged_decode_step_launches.restype = c_i32
+_lib.lnk_paged_decode_step_launches.argtypes = [ctypes.POINTER(AttnDesc), c_i32]
 _lib.lnk_paged_decode_attn_static.restype = ctypes.c_int
 _lib.lnk_paged_decode_attn_static.argtypes = [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                               c_i32, c_vp, c_vp]
@@ -167,6 +174,20 @@ def lnk_paged_decode_attn(desc, q_roped, positions, table, k_pool, v_pool, out, 
                                     _ptr(k_pool), _ptr(v_pool), _ptr(out), B, _ptr(workspace),
                                     ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "lnk_paged_decode_attn")
+
+
+def lnk_paged_decode_step(desc, rope, q, k, v, positions, table, q_norm_w, k_norm_w, norm_eps, k_pool,
+                          v_pool, q_out, out, B, workspace, ws_bytes, dev_status=None, stream=None):
+    st = _lib.lnk_paged_decode_step(ctypes.byref(desc), ctypes.byref(rope), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(positions), _ptr(table), _ptr(q_norm_w), _ptr(k_norm_w), norm_eps,
+                                    _ptr(k_pool), _ptr(v_pool), _ptr(q_out), _ptr(out), B, _ptr(workspace),
+                                    ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(st, "lnk_paged_decode_step")
+
+
+def lnk_paged_decode_step_launches(desc, B) -> int:
+    """Kernels lnk_paged_decode_step enqueues for B rows (1 or 2; 0 for B = 0; -1: rejected)."""
+    return int(_lib.lnk_paged_decode_step_launches(ctypes.byref(desc), B))
 
 
 def lnk_paged_decode_attn_static(desc, q_roped, positions, table, k_pool, v_pool, out, B,

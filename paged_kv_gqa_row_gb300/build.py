@@ -22,7 +22,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr
 LIBS = {
     "lnk": {
         "sources": [os.path.join(CSRC, f) for f in ("api.cu", "append_rope.cu", "decode.cu", "chunk.cu", "decode_static.cu", "pages.cu", "selftest.cu", "pager.cpp")],
-        "headers": [os.path.join(CSRC, f) for f in ("common.cuh", "ptx.cuh")] + [os.path.join(INCLUDE, "lnk.h")],
+        "headers": [os.path.join(CSRC, f) for f in ("common.cuh", "ptx.cuh", "rope_math.cuh")] + [os.path.join(INCLUDE, "lnk.h")],
         "out": os.path.join(PKG, "liblnk.so"),
     },
     "synth": {

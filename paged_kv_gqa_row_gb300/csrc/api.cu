@@ -1,5 +1,6 @@
 // C ABI entry points of liblnk: argument checks, frequency tables, tensor
 // maps and launches.  Nothing here allocates device memory or synchronises.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <cstring>
@@ -250,16 +251,17 @@ size_t lnk_paged_workspace_size(const lnk_attn_desc* desc, int32_t max_rows) {
       .total;
 }
 
-lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope, const lnk_bf16* q,
-                                 const lnk_bf16* k, const lnk_bf16* v, const int32_t* positions,
-                                 const int32_t* rows, const int32_t* slots, const int32_t* table,
-                                 const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w, float norm_eps,
-                                 lnk_bf16* k_pool, lnk_bf16* v_pool, lnk_bf16* q_out, int32_t T,
-                                 int32_t* dev_status, lnk_stream stream) {
-  lnk_status st = check_desc(desc);
-  if (st != LNK_OK) return st;
-  if (T < 0) return LNK_EINVAL;
-  if (T == 0) return LNK_OK;
+}  // extern "C"
+
+namespace lnk {
+
+// Checks the append's arguments and fills its kernel parameters (shared by
+// lnk_paged_append_rope and the fused decode step).  T > 0.
+static lnk_status append_params(const lnk_attn_desc* desc, const lnk_rope_desc* rope, const lnk_bf16* q,
+                                const lnk_bf16* k, const lnk_bf16* v, const int32_t* positions, const int32_t* rows,
+                                const int32_t* slots, const int32_t* table, const lnk_bf16* q_norm_w,
+                                const lnk_bf16* k_norm_w, float norm_eps, lnk_bf16* k_pool, lnk_bf16* v_pool,
+                                lnk_bf16* q_out, int32_t T, int32_t* dev_status, AppendParams* out) {
   if (!q || !k || !v || !positions || !k_pool || !v_pool || !q_out) return LNK_EINVAL;
   if (slots == nullptr && table == nullptr) return LNK_EINVAL;
   if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 16) || !aligned(q_out, 4) || !aligned(k_pool, 16) ||
@@ -267,7 +269,7 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
     return LNK_EINVAL;
   if ((q_norm_w || k_norm_w) && !(norm_eps >= 0.f)) return LNK_EINVAL;
   if (rows == nullptr && slots == nullptr && T > desc->num_rows) return LNK_EINVAL;
-  AppendParams p;
+  AppendParams& p = *out;
   std::memset(&p, 0, sizeof(p));
   {
     // the table is the same step after step: keep the last one per thread
@@ -284,7 +286,7 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
                                         c.rope.high_freq_factor == rope->high_freq_factor &&
                                         c.rope.original_max_position == rope->original_max_position));
     if (!hit) {
-      st = inv_freq_table(rope, desc->head_dim, c.table);
+      const lnk_status st = inv_freq_table(rope, desc->head_dim, c.table);
       if (st != LNK_OK) {
         c.valid = false;
         return st;
@@ -318,6 +320,28 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
   p.kv8 = desc->kv_dtype == LNK_KV_E4M3;
   p.k_scale = desc->k_scale;
   p.v_scale = desc->v_scale;
+  p.splits = 1;
+  return LNK_OK;
+}
+
+}  // namespace lnk
+
+extern "C" {
+
+lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc* rope, const lnk_bf16* q,
+                                 const lnk_bf16* k, const lnk_bf16* v, const int32_t* positions,
+                                 const int32_t* rows, const int32_t* slots, const int32_t* table,
+                                 const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w, float norm_eps,
+                                 lnk_bf16* k_pool, lnk_bf16* v_pool, lnk_bf16* q_out, int32_t T,
+                                 int32_t* dev_status, lnk_stream stream) {
+  lnk_status st = check_desc(desc);
+  if (st != LNK_OK) return st;
+  if (T < 0) return LNK_EINVAL;
+  if (T == 0) return LNK_OK;
+  AppendParams p;
+  st = append_params(desc, rope, q, k, v, positions, rows, slots, table, q_norm_w, k_norm_w, norm_eps, k_pool,
+                     v_pool, q_out, T, dev_status, &p);
+  if (st != LNK_OK) return st;
   return launch_append(p, desc->head_dim, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? LNK_OK
                                                                                                 : LNK_ECUDA;
 }
@@ -326,10 +350,12 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
 // clear_counters: zero the workspace's counters on the stream right before the
 // launch (after every check has passed), for a workspace whose previous
 // contents are unknown.
+// fuse: the fused decode step's append parameters (null: attention only).
 static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, const int32_t* positions,
                                 const int32_t* table, lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes,
                                 int32_t* dev_status, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                cudaStream_t stream, bool clear_counters = false) {
+                                cudaStream_t stream, bool clear_counters = false,
+                                const AppendParams* fuse = nullptr) {
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
@@ -358,6 +384,12 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   p.window = desc->window;
   p.scale_log2 = scale_log2(desc);
   p.out_scale = kv8 ? desc->v_scale : 1.f;
+  std::memset(&p.ap, 0, sizeof(p.ap));
+  p.fuse = 0;
+  if (fuse != nullptr) {
+    p.fuse = 1;
+    p.ap = *fuse;
+  }
   if (clear_counters && cudaMemsetAsync(ws, 0, w.ml, stream) != cudaSuccess) return LNK_ECUDA;
   return launch_decode(kmap, vmap, p, desc->head_dim, launch, stream) == cudaSuccess ? LNK_OK : LNK_ECUDA;
 }
@@ -393,6 +425,62 @@ lnk_status lnk_paged_decode_attn(const lnk_attn_desc* desc, const lnk_bf16* q_ro
                                  lnk_stream stream) {
   return decode_entry(desc, q_roped, positions, table, k_pool, v_pool, out, B, workspace, ws_bytes, dev_status,
                       stream, false);
+}
+
+// The decode step is one kernel when every (row, kv head) pair can be one
+// CTA's only work and the pairs occupy at least half the SMs, with at most
+// kFuseMaxPages pages a pair (so that one long pair cannot hold up the launch
+// for long).
+static bool decode_step_fuses(const lnk_attn_desc* desc, int32_t B, int grid) {
+  const long long pairs = static_cast<long long>(B) * desc->num_kv_heads;
+  long long pair_pages = desc->pages_per_row;
+  if (desc->window > 0) pair_pages = std::min<long long>(pair_pages, (desc->window - 1) / kPage + 2);
+  return pairs <= grid && 2 * pairs >= device_sm_count() && pair_pages <= kFuseMaxPages;
+}
+
+int32_t lnk_paged_decode_step_launches(const lnk_attn_desc* desc, int32_t B) {
+  if (check_desc(desc) != LNK_OK || B < 0 || B > desc->num_rows || B > kMaxDecodeRows) return -1;
+  if (B == 0) return 0;
+  DecodeLaunch launch;
+  if (decode_prepare(desc->head_dim, desc->kv_dtype == LNK_KV_E4M3, B, desc->num_kv_heads, &launch) !=
+          cudaSuccess ||
+      launch.grid <= 0)
+    return -1;
+  return decode_step_fuses(desc, B, launch.grid) ? 1 : 2;
+}
+
+lnk_status lnk_paged_decode_step(const lnk_attn_desc* desc, const lnk_rope_desc* rope, const lnk_bf16* q,
+                                 const lnk_bf16* k, const lnk_bf16* v, const int32_t* positions,
+                                 const int32_t* table, const lnk_bf16* q_norm_w, const lnk_bf16* k_norm_w,
+                                 float norm_eps, lnk_bf16* k_pool, lnk_bf16* v_pool, lnk_bf16* q_out,
+                                 lnk_bf16* out, int32_t B, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 lnk_stream stream) {
+  lnk_status st = check_desc(desc);
+  if (st != LNK_OK) return st;
+  if (B < 0 || B > desc->num_rows) return LNK_EINVAL;
+  if (B > kMaxDecodeRows) return LNK_ERANGE;
+  if (B == 0) return LNK_OK;
+  if (!table || !out || !aligned(q_out, 16) || !aligned(out, 8)) return LNK_EINVAL;
+  AppendParams ap;
+  st = append_params(desc, rope, q, k, v, positions, nullptr, nullptr, table, q_norm_w, k_norm_w, norm_eps, k_pool,
+                     v_pool, q_out, B, dev_status, &ap);
+  if (st != LNK_OK) return st;
+  CUtensorMap kmap, vmap;
+  if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
+  DecodeLaunch launch;
+  const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
+  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch) != cudaSuccess || launch.grid <= 0)
+    return LNK_ECUDA;
+  const int group = desc->num_q_heads / desc->num_kv_heads;
+  const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
+  if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 256)) return LNK_EWORKSPACE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (decode_step_fuses(desc, B, launch.grid))
+    return decode_common(desc, q_out, positions, table, out, B, workspace, ws_bytes, dev_status, kmap, vmap, s,
+                         false, &ap);
+  // otherwise the append, then attention
+  if (launch_append(ap, desc->head_dim, s) != cudaSuccess) return LNK_ECUDA;
+  return decode_common(desc, q_out, positions, table, out, B, workspace, ws_bytes, dev_status, kmap, vmap, s);
 }
 
 lnk_status lnk_paged_step_attn(const lnk_attn_desc* desc, const lnk_bf16* q_roped, const int32_t* rows,

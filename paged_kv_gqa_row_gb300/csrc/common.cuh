@@ -37,6 +37,7 @@ struct AppendParams {
   int T, hq, hkv, num_pages, num_rows, pages_per_row;
   int kv8;                    // pools hold E4M3 codes
   float k_scale, v_scale;     // their scales (a code c stands for e4m3(c) * scale)
+  int splits;                 // CTAs per token (set by launch_append)
   float inv_freq[64];
 };
 
@@ -56,6 +57,12 @@ struct DecodeParams {
   int B, hq, hkv, group, num_pages, pages_per_row, window;
   float scale_log2;           // softmax scale * log2(e) (8-bit pools: times the key scale)
   float out_scale;            // 1, or the value scale of an 8-bit pool
+  // Fused decode step (fuse != 0): the CTA of pair (b, h) first rotates and
+  // writes row b's token for kv head h (the append's work for that pair, with
+  // `ap`: T = B, token b in table row b) and then attends.  Set only when every
+  // pair is one CTA's single chunk.
+  int fuse;
+  AppendParams ap;
 };
 
 struct DecodeLaunch {
@@ -69,6 +76,7 @@ struct DecodeWorkspace {
   size_t next, count, ml, o, total;  // the counters (next, count) come first and must start at zero
 };
 constexpr int kChunksPerCta = 4;  // decode work chunks per persistent CTA
+constexpr int kFuseMaxPages = 16;  // fused decode step: at most this many pages a (row, kv head) pair
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
 cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch);

@@ -53,9 +53,11 @@
 //    in that same order, so P^T from movmatrix matches; the 4 dimensions a
 //    lane holds make the M rows of two d-tiles, undone when O is staged.
 // The key scale multiplies the softmax scale, the value scale the output.
-// The per-row prologue (visible pages, prefix sums) reads only positions, so
-// it overlaps the previous kernel on the stream (programmatic dependent
-// launch); the kernel waits for that kernel before touching q or the pool.
+// The per-row prologue (visible pages, prefix sums, the producer's plan of its
+// first chunk) reads only positions and the table, so it overlaps the
+// previous kernel on the stream (programmatic dependent launch); the kernel
+// waits for that kernel before touching q or the pool.  It lets the next
+// kernel on the stream start early in the same way.
 //
 // Sources: "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
 // (decode_rows: a row attends over itself up to its position; window_mask;
@@ -63,6 +65,7 @@
 // (decode_paged: the pool, pages of 64, table[b]).
 #include "common.cuh"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace lnk {
 namespace {
@@ -101,7 +104,9 @@ struct DecodeSmem {
   static constexpr size_t stages = 0;
   static constexpr size_t qbuf = stages + size_t(kStages) * kStageBytes;
   static constexpr size_t bars = qbuf + size_t(kStages) * kQBytes;
-  static constexpr size_t info = bars + (2 * kStages + 4) * sizeof(uint64_t);
+  // full[kStages], empty[kStages], slot_full[2], slot_empty[2], appended
+  // (rounded up to 16 bytes: the staging slots after them are read as float4)
+  static constexpr size_t info = bars + ((2 * kStages + 5) * sizeof(uint64_t) + 15) / 16 * 16;
   static constexpr size_t slot_info = info + kStages * sizeof(StageInfo);
   static constexpr size_t ostage = slot_info + 2 * sizeof(StageInfo);
   static constexpr size_t mstage = ostage + 2 * size_t(kSlotFloats) * 4;
@@ -109,6 +114,13 @@ struct DecodeSmem {
   static constexpr size_t epi = lstage + 2 * kConsumerWarps * kMaxGroup * 4;   // epilogue scratch
   static constexpr size_t misc = epi + 2 * kMaxGroup * 4;                       // abort flag, scan sums
   static constexpr size_t pref = misc + 64;
+  // Fused decode step: the rotation coefficients [2 kinds][D / 2] live in the
+  // epilogue's staging slots, which nothing writes before the pair's last page
+  // has landed (that page waits for the append, the append's last reader of
+  // the coefficients).
+  static constexpr size_t coef = ostage;
+  static_assert(2 * (D / 2) * sizeof(rope::Coefs) <= 2 * size_t(kSlotFloats) * 4, "coefficients fit the staging slots");
+  static_assert(ostage % 16 == 0 && kOStride % 4 == 0, "staging rows are read as float4");
   static size_t bytes(int B) { return pref + size_t(B + 1) * 4 + 1024; }  // + alignment slack
 };
 
@@ -169,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* slot_full = empty_bar + kStages;  // [2]: consumer warps -> epilogue
   uint64_t* slot_empty = slot_full + 2;       // [2]: epilogue -> consumer warps
+  uint64_t* appended = slot_empty + 2;        // fused step: the pair's new K/V row is in the pool
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::info);
   StageInfo* slot_info = reinterpret_cast<StageInfo*>(smem + L::slot_info);
   float* ost = reinterpret_cast<float*>(smem + L::ostage);
@@ -177,6 +190,11 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   int* misc = reinterpret_cast<int*>(smem + L::misc);  // [0] abort, [2..7] warp sums of the scan, [8] longest pair
   volatile int* abort_flag = misc;
   int* pref = reinterpret_cast<int*>(smem + L::pref);
+
+  // Let the next kernel on the stream start its own prologue while this one
+  // runs; it must wait for this grid (griddepcontrol.wait) before it reads
+  // the output or writes anything this kernel reads.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -193,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       mbar_init(smem_addr(slot_full + i), kConsumerWarps);
       mbar_init(smem_addr(slot_empty + i), 1);
     }
+    mbar_init(smem_addr(appended), 1);
     misc[0] = 0;
     misc[8] = 0;  // longest pair (pages)
     fence_mbarrier_init();
@@ -234,7 +253,10 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   const long long pairs = static_cast<long long>(B) * p.hkv;
   // At most one pair per CTA, none longer than twice a CTA's share: each
   // chunk is one whole pair (no partial results, no merges).
-  const bool pair_chunks = pairs <= gridDim.x && 2 * ((total + gridDim.x - 1) / gridDim.x) >= misc[8];
+  // (The fused step always takes one pair per CTA: the host calls it only when
+  // the pairs fit the grid and are short.)
+  const bool pair_chunks =
+      p.fuse || (pairs <= gridDim.x && 2 * ((total + gridDim.x - 1) / gridDim.x) >= misc[8]);
   // Several chunks per CTA only when pairs are many (and so short) against a
   // CTA's share: each chunk boundary cuts a pair, and a cut pair costs a
   // partial result and a merge.
@@ -255,6 +277,62 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     }
   };
 
+  // The producer's plan of a chunk: its page-head range, the order of its
+  // segments (the one it shares with the next chunk first), the cursor at the
+  // first page-head and that page's table entry.
+  struct ChunkPlan {
+    long long start, end, r_begin[2], r_end[2];
+    int nranges, page;
+    Cursor cur;
+  };
+  auto plan_chunk = [&](long long chunk, ChunkPlan& pl) {
+    chunk_range(chunk, pl.start, pl.end);
+    pl.nranges = 0;
+    if (pl.start >= pl.end) return;
+    locate(pl.cur, pl.end - 1, pref, p, pl.start, pl.end, per, chunk);
+    const long long last_seg = max(pl.start, pl.end - 1 - pl.cur.j);
+    const bool last_cut = (pl.end - 1 - pl.cur.j) + pl.cur.np > pl.end;
+    if (last_cut && last_seg > pl.start) {
+      pl.r_begin[0] = last_seg; pl.r_end[0] = pl.end;
+      pl.r_begin[1] = pl.start; pl.r_end[1] = last_seg;
+      pl.nranges = 2;
+    } else {
+      pl.r_begin[0] = pl.start; pl.r_end[0] = pl.end;
+      pl.nranges = 1;
+    }
+    locate(pl.cur, pl.r_begin[0], pref, p, pl.start, pl.end, per, chunk);
+    pl.page = pl.cur.trow[pl.cur.first_page + pl.cur.j];
+  };
+  // Fused step, before the wait (positions and the table only): the sine and
+  // cosine of row b's angles (threads below D / 2) and the pool slot of its
+  // token (the epilogue warp's last lane) for this CTA's pair (b, h).
+  constexpr int H = D / 2;
+  const bool fused = p.fuse && static_cast<long long>(blockIdx.x) < pairs;
+  const int f_row = fused ? static_cast<int>(blockIdx.x / p.hkv) : 0;
+  const int f_head = fused ? static_cast<int>(blockIdx.x % p.hkv) : 0;
+  const int fpos = fused ? p.positions[f_row] : -1;
+  rope::DF f_sn{0.f, 0.f}, f_cs{0.f, 0.f};
+  if (fused && tid < H && fpos >= 0) rope::angle_sincos(fpos, p.ap.inv_freq[tid], f_sn, f_cs);
+  long long f_slot = -1;
+  int f_bad = 0;
+  if (fused && warp == kEpilogueWarp && lane == 31 && fpos >= 0) {
+    if (fpos >= p.pages_per_row * kPage) {
+      f_bad = LNK_DEV_BAD_POSITION;
+    } else {
+      const int page = p.table[static_cast<long long>(f_row) * p.pages_per_row + fpos / kPage];
+      if (page < 0 || page >= p.num_pages) f_bad = LNK_DEV_BAD_PAGE;
+      else f_slot = static_cast<long long>(page) * kPage + fpos % kPage;
+    }
+  }
+
+  // The first chunk's plan reads only positions and the table, so the
+  // producer makes it before the wait (neither may be written by the
+  // previous kernel on the stream).
+  ChunkPlan first_plan;
+  first_plan.nranges = 0;
+  if (warp == kProducerWarp && lane == 0 && static_cast<long long>(blockIdx.x) < nchunks)
+    plan_chunk(blockIdx.x, first_plan);
+
   // Wait for the previous kernel on the stream (it writes q and the pool).
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -267,39 +345,131 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   }
   if (static_cast<long long>(blockIdx.x) >= nchunks) return;
 
+  // ---- fused step: the append's work for this CTA's pair (b, h) ----
+  // Consumer warp w rotates query heads w, w + 4 of the pair into q_out and
+  // into stage 0's query rows; the epilogue warp rotates the key head into
+  // the pool slot and copies the value row there, then tells the producer,
+  // which loads the pair's last page (the one holding the slot) only after
+  // that.  The arithmetic is rope_math.cuh's, as in the append kernel.
+  if (fused && warp != kProducerWarp) {
+    rope::Coefs* s_coef = reinterpret_cast<rope::Coefs*>(smem + L::coef);  // [queries, keys][D / 2]
+    const AppendParams& ap = p.ap;
+    if (tid < H && fpos >= 0) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* w = which == 0 ? ap.q_norm_w : ap.k_norm_w;
+        float g1 = 1.f, g2 = 1.f;
+        if (w != nullptr) {
+          g1 = __uint_as_float(static_cast<uint32_t>(w[tid]) << 16);
+          g2 = __uint_as_float(static_cast<uint32_t>(w[tid + H]) << 16);
+        }
+        s_coef[which * H + tid] = rope::coefs_of(f_sn, f_cs, g1, g2);
+      }
+    }
+    named_barrier_sync(1, (kConsumerWarps + 1) * 32);  // the consumer warps and the epilogue warp
+    const bool has = lane < D / 4;  // lanes holding elements (e, e + 1) and (e + D/2, e + D/2 + 1)
+    const int e = 2 * lane;
+    const bool live = fpos >= 0;
+    if (warp < kConsumerWarps) {
+      uint16_t* sq = reinterpret_cast<uint16_t*>(smem + L::qbuf);  // stage 0's query rows [G][D]
+      const bool normed = ap.q_norm_w != nullptr;
+      for (int g = warp; g < G; g += kConsumerWarps) {
+        const size_t row = (static_cast<size_t>(f_row) * p.hq + static_cast<size_t>(f_head) * G + g) * D;
+        uint32_t xlo = 0u, xhi = 0u;
+        if (has && live) {
+          xlo = *reinterpret_cast<const uint32_t*>(ap.q + row + e);
+          xhi = *reinterpret_cast<const uint32_t*>(ap.q + row + H + e);
+        }
+        rope::DF r{1.f, 0.f};
+        if (normed && live) r = rope::rms_factor(rope::head_sumsq(xlo, xhi), D, ap.norm_eps);
+        uint32_t lo = 0u, hi = 0u;  // (zero for an inactive row)
+        if (has && live) rope::rotate_pairs(xlo, xhi, s_coef, e, normed, r, lo, hi);
+        if (has) {
+          *reinterpret_cast<uint32_t*>(ap.q_out + row + e) = lo;
+          *reinterpret_cast<uint32_t*>(ap.q_out + row + H + e) = hi;
+          *reinterpret_cast<uint32_t*>(sq + g * D + e) = lo;
+          *reinterpret_cast<uint32_t*>(sq + g * D + H + e) = hi;
+        }
+      }
+      named_barrier_sync(2, kConsumerWarps * 32);  // every query row is in shared memory
+    } else {
+      const long long slot = __shfl_sync(0xffffffffu, f_slot, 31);
+      if (lane == 31 && f_bad && p.status != nullptr) atomicOr(p.status, f_bad);
+      if (slot >= 0) {
+        const size_t src = (static_cast<size_t>(f_row) * p.hkv + f_head) * D;
+        const size_t dst = (static_cast<size_t>(f_head) * p.num_pages * kPage + static_cast<size_t>(slot)) * D;
+        const bool normed = ap.k_norm_w != nullptr;
+        uint32_t xlo = 0u, xhi = 0u;
+        if (has) {
+          xlo = *reinterpret_cast<const uint32_t*>(ap.k + src + e);
+          xhi = *reinterpret_cast<const uint32_t*>(ap.k + src + H + e);
+        }
+        rope::DF r{1.f, 0.f};
+        if (normed) r = rope::rms_factor(rope::head_sumsq(xlo, xhi), D, ap.norm_eps);
+        if (has) {
+          uint32_t lo, hi;
+          rope::rotate_pairs(xlo, xhi, s_coef + H, e, normed, r, lo, hi);
+          if (ap.kv8) {
+            uint8_t* k8 = reinterpret_cast<uint8_t*>(ap.k_pool) + dst;
+            *reinterpret_cast<uint16_t*>(k8 + e) = rope::e4m3_pair(lo, ap.k_scale);
+            *reinterpret_cast<uint16_t*>(k8 + H + e) = rope::e4m3_pair(hi, ap.k_scale);
+          } else {
+            *reinterpret_cast<uint32_t*>(ap.k_pool + dst + e) = lo;
+            *reinterpret_cast<uint32_t*>(ap.k_pool + dst + H + e) = hi;
+          }
+        }
+        if (lane < D / 8) {
+          const uint4 x = reinterpret_cast<const uint4*>(ap.v + src)[lane];
+          if (ap.kv8) {
+            uint2 codes;
+            codes.x = rope::e4m3_pair(x.x, ap.v_scale) | (static_cast<uint32_t>(rope::e4m3_pair(x.y, ap.v_scale)) << 16);
+            codes.y = rope::e4m3_pair(x.z, ap.v_scale) | (static_cast<uint32_t>(rope::e4m3_pair(x.w, ap.v_scale)) << 16);
+            reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(ap.v_pool) + dst)[lane] = codes;
+          } else {
+            reinterpret_cast<uint4*>(ap.v_pool + dst)[lane] = x;
+          }
+        }
+        // the producer's tensor copies (async proxy) read these rows next
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(appended));
+    }
+  }
+
   if (warp == kProducerWarp) {
     // ============================== producer ==============================
     if (lane != 0) return;
-    const uint32_t q_bytes = static_cast<uint32_t>(G * D * 2);
+    // (fused step: the consumers write the rotated queries themselves)
+    const uint32_t q_bytes = fused ? 0u : static_cast<uint32_t>(G * D * 2);
     int k = 0;
     bool stop = false;
     Cursor cur;
     for (long long chunk = blockIdx.x; chunk < nchunks && !stop;) {
-      long long start, end;
-      chunk_range(chunk, start, end);
-      if (start < end) {
-      // Order: the chunk's last segment first when its pair continues into the
-      // next chunk, then everything else in stream order.
-      locate(cur, end - 1, pref, p, start, end, per, chunk);
-      const long long last_seg = max(start, end - 1 - cur.j);
-      const bool last_cut = (end - 1 - cur.j) + cur.np > end;
-      long long r_begin[2], r_end[2];
-      int nranges = 1;
-      if (last_cut && last_seg > start) {
-        r_begin[0] = last_seg; r_end[0] = end;
-        r_begin[1] = start;    r_end[1] = last_seg;
-        nranges = 2;
-      } else {
-        r_begin[0] = start; r_end[0] = end;
-      }
-      for (int rg = 0; rg < nranges && !stop; ++rg) {
-        locate(cur, r_begin[rg], pref, p, start, end, per, chunk);
+      ChunkPlan pl;
+      if (chunk == blockIdx.x) pl = first_plan; else plan_chunk(chunk, pl);
+      const long long start = pl.start, end = pl.end;
+      const long long* r_begin = pl.r_begin;
+      const long long* r_end = pl.r_end;
+      for (int rg = 0; rg < pl.nranges && !stop; ++rg) {
         // the page of the next step is read one step ahead, so that the table's
         // latency overlaps the wait for a free stage
-        int next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
+        int next_page = pl.page;
+        if (rg == 0) {
+          cur = pl.cur;
+        } else {
+          locate(cur, r_begin[rg], pref, p, start, end, per, chunk);
+          next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
+        }
         for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
           const int s = k % kStages;
           if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          // fused step: the pair's last page holds the new token, written by
+          // the epilogue warp; load it only after that write
+          if (fused && cur.j == cur.np - 1 && !mbar_wait(smem_addr(appended), 0, abort_flag)) {
             stop = true;
             break;
           }
@@ -325,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           const uint32_t fb = smem_addr(full_bar + s);
           const uint32_t tx = (valid ? static_cast<uint32_t>(L::kStageBytes) : 0u) + (first ? q_bytes : 0u);
           if (tx) mbar_arrive_expect_tx(fb, tx); else mbar_arrive(fb);
-          if (first) {
+          if (first && q_bytes > 0) {
             const uint16_t* qsrc = p.q + (static_cast<size_t>(cur.b) * p.hq + static_cast<size_t>(cur.h) * G) * D;
             bulk_load(smem_addr(smem + L::qbuf + size_t(s) * L::kQBytes), qsrc, q_bytes, fb);
           }
@@ -344,9 +514,10 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
         }
       }
-      }
       // the next chunk: claims are handed out in order, nchunks in all; the
-      // last claimant returns the counter to zero for the next launch
+      // last claimant returns the counter to zero for the next launch (with
+      // no more chunks than CTAs there is nothing to claim)
+      if (nchunks <= static_cast<long long>(gridDim.x)) break;
       const int v = atomicAdd(p.ws_next, 1);
       if (v == static_cast<int>(nchunks) - 1) atomicExch(p.ws_next, 0);
       chunk = static_cast<long long>(v) + gridDim.x;
