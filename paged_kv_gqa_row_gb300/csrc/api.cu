@@ -359,7 +359,8 @@ static lnk_status decode_common(const lnk_attn_desc* desc, const lnk_bf16* q, co
   if (B == 0) return LNK_OK;
   DecodeLaunch launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
-  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch) != cudaSuccess || launch.grid <= 0)
+  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch, fuse != nullptr) != cudaSuccess ||
+      launch.grid <= 0)
     return LNK_ECUDA;
   const int group = desc->num_q_heads / desc->num_kv_heads;
   const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
@@ -442,7 +443,7 @@ int32_t lnk_paged_decode_step_launches(const lnk_attn_desc* desc, int32_t B) {
   if (check_desc(desc) != LNK_OK || B < 0 || B > desc->num_rows || B > kMaxDecodeRows) return -1;
   if (B == 0) return 0;
   DecodeLaunch launch;
-  if (decode_prepare(desc->head_dim, desc->kv_dtype == LNK_KV_E4M3, B, desc->num_kv_heads, &launch) !=
+  if (decode_prepare(desc->head_dim, desc->kv_dtype == LNK_KV_E4M3, B, desc->num_kv_heads, &launch, true) !=
           cudaSuccess ||
       launch.grid <= 0)
     return -1;
@@ -467,15 +468,21 @@ lnk_status lnk_paged_decode_step(const lnk_attn_desc* desc, const lnk_rope_desc*
   if (st != LNK_OK) return st;
   CUtensorMap kmap, vmap;
   if (!pool_map(&kmap, k_pool, *desc) || !pool_map(&vmap, v_pool, *desc)) return LNK_ECUDA;
-  DecodeLaunch launch;
+  // the launch of the one-kernel form, and the attention kernel's launch of
+  // the two-kernel form
+  DecodeLaunch fused_launch, launch;
   const bool kv8 = desc->kv_dtype == LNK_KV_E4M3;
-  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch) != cudaSuccess || launch.grid <= 0)
+  if (decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &fused_launch, true) != cudaSuccess ||
+      fused_launch.grid <= 0 ||
+      decode_prepare(desc->head_dim, kv8, B, desc->num_kv_heads, &launch) != cudaSuccess || launch.grid <= 0)
     return LNK_ECUDA;
   const int group = desc->num_q_heads / desc->num_kv_heads;
-  const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim, launch.grid);
+  const bool fuses = decode_step_fuses(desc, B, fused_launch.grid);
+  const DecodeWorkspace w = decode_workspace_layout(B, desc->num_kv_heads, group, desc->head_dim,
+                                                    fuses ? fused_launch.grid : launch.grid);
   if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 256)) return LNK_EWORKSPACE;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (decode_step_fuses(desc, B, launch.grid))
+  if (fuses)
     return decode_common(desc, q_out, positions, table, out, B, workspace, ws_bytes, dev_status, kmap, vmap, s,
                          false, &ap);
   // otherwise the append, then attention

@@ -79,7 +79,8 @@ constexpr int kChunksPerCta = 4;  // decode work chunks per persistent CTA
 constexpr int kFuseMaxPages = 16;  // fused decode step: at most this many pages a (row, kv head) pair
 DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_dim, int grid);
 
-cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch);
+// fused: the launch of the one-kernel decode step (two CTAs per SM when they fit)
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch, bool fused = false);
 
 // lnk_paged_decode_attn with an option: clear_counters zeroes the workspace's
 // counters on the stream once every argument check has passed, right before

@@ -277,12 +277,24 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     }
   };
 
+  // The table entries of the cursor's page and of the pair's next three
+  // pages (0 past the pair's last page), read together: the producer keeps
+  // this window of entries, so that a page's TMA copies never wait for the
+  // table once the window is full.
+  auto window_entries = [&](const Cursor& c, int& e0, int& e1, int& e2, int& e3) {
+    const int* t = c.trow + c.first_page + c.j;
+    const int left = c.np - c.j;
+    e0 = left > 0 ? t[0] : 0;
+    e1 = left > 1 ? t[1] : 0;
+    e2 = left > 2 ? t[2] : 0;
+    e3 = left > 3 ? t[3] : 0;
+  };
   // The producer's plan of a chunk: its page-head range, the order of its
   // segments (the one it shares with the next chunk first), the cursor at the
-  // first page-head and that page's table entry.
+  // first page-head and the window of table entries there.
   struct ChunkPlan {
-    long long start, end, r_begin[2], r_end[2];
-    int nranges, page;
+    long long start, end, rb0, re0, rb1, re1;  // ranges in order: [rb0, re0), then [rb1, re1)
+    int nranges, e0, e1, e2, e3;
     Cursor cur;
   };
   auto plan_chunk = [&](long long chunk, ChunkPlan& pl) {
@@ -293,15 +305,16 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     const long long last_seg = max(pl.start, pl.end - 1 - pl.cur.j);
     const bool last_cut = (pl.end - 1 - pl.cur.j) + pl.cur.np > pl.end;
     if (last_cut && last_seg > pl.start) {
-      pl.r_begin[0] = last_seg; pl.r_end[0] = pl.end;
-      pl.r_begin[1] = pl.start; pl.r_end[1] = last_seg;
+      pl.rb0 = last_seg; pl.re0 = pl.end;
+      pl.rb1 = pl.start; pl.re1 = last_seg;
       pl.nranges = 2;
     } else {
-      pl.r_begin[0] = pl.start; pl.r_end[0] = pl.end;
+      pl.rb0 = pl.start; pl.re0 = pl.end;
+      pl.rb1 = pl.re1 = pl.end;
       pl.nranges = 1;
     }
-    locate(pl.cur, pl.r_begin[0], pref, p, pl.start, pl.end, per, chunk);
-    pl.page = pl.cur.trow[pl.cur.first_page + pl.cur.j];
+    locate(pl.cur, pl.rb0, pref, p, pl.start, pl.end, per, chunk);
+    window_entries(pl.cur, pl.e0, pl.e1, pl.e2, pl.e3);
   };
   // Fused step, before the wait (positions and the table only): the sine and
   // cosine of row b's angles (threads below D / 2) and the pool slot of its
@@ -399,11 +412,14 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
         const size_t src = (static_cast<size_t>(f_row) * p.hkv + f_head) * D;
         const size_t dst = (static_cast<size_t>(f_head) * p.num_pages * kPage + static_cast<size_t>(slot)) * D;
         const bool normed = ap.k_norm_w != nullptr;
+        // (the key and value rows are loaded together, before any store)
         uint32_t xlo = 0u, xhi = 0u;
+        uint4 vx = make_uint4(0u, 0u, 0u, 0u);
         if (has) {
           xlo = *reinterpret_cast<const uint32_t*>(ap.k + src + e);
           xhi = *reinterpret_cast<const uint32_t*>(ap.k + src + H + e);
         }
+        if (lane < D / 8) vx = reinterpret_cast<const uint4*>(ap.v + src)[lane];
         rope::DF r{1.f, 0.f};
         if (normed) r = rope::rms_factor(rope::head_sumsq(xlo, xhi), D, ap.norm_eps);
         if (has) {
@@ -419,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           }
         }
         if (lane < D / 8) {
-          const uint4 x = reinterpret_cast<const uint4*>(ap.v + src)[lane];
+          const uint4 x = vx;
           if (ap.kv8) {
             uint2 codes;
             codes.x = rope::e4m3_pair(x.x, ap.v_scale) | (static_cast<uint32_t>(rope::e4m3_pair(x.y, ap.v_scale)) << 16);
@@ -449,19 +465,16 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
       ChunkPlan pl;
       if (chunk == blockIdx.x) pl = first_plan; else plan_chunk(chunk, pl);
       const long long start = pl.start, end = pl.end;
-      const long long* r_begin = pl.r_begin;
-      const long long* r_end = pl.r_end;
       for (int rg = 0; rg < pl.nranges && !stop; ++rg) {
-        // the page of the next step is read one step ahead, so that the table's
-        // latency overlaps the wait for a free stage
-        int next_page = pl.page;
+        const long long rb = rg == 0 ? pl.rb0 : pl.rb1, re = rg == 0 ? pl.re0 : pl.re1;
+        int e0 = pl.e0, e1 = pl.e1, e2 = pl.e2, e3 = pl.e3;  // table window at the cursor
         if (rg == 0) {
           cur = pl.cur;
         } else {
-          locate(cur, r_begin[rg], pref, p, start, end, per, chunk);
-          next_page = r_begin[rg] < r_end[rg] ? cur.trow[cur.first_page + cur.j] : 0;
+          locate(cur, rb, pref, p, start, end, per, chunk);
+          window_entries(cur, e0, e1, e2, e3);
         }
-        for (long long gi = r_begin[rg]; gi < r_end[rg]; ++gi, ++k) {
+        for (long long gi = rb; gi < re; ++gi, ++k) {
           const int s = k % kStages;
           if (k >= kStages && !mbar_wait(smem_addr(empty_bar + s), ((k / kStages) - 1) & 1, abort_flag)) {
             stop = true;
@@ -474,14 +487,14 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
             break;
           }
           const int lp = cur.first_page + cur.j;
-          const int page = next_page;
+          const int page = e0;
           StageInfo si;
           si.b = cur.b;
           si.h = cur.h;
           si.klo = max(cur.lo - lp * kPage, 0);
           si.khi = min(cur.pos - lp * kPage + 1, kPage);
-          const bool first = gi == r_begin[rg] || cur.j == 0;
-          si.flags = (first ? kSegFirst : 0) | ((gi == r_end[rg] - 1 || cur.j == cur.np - 1) ? kSegLast : 0) |
+          const bool first = gi == rb || cur.j == 0;
+          si.flags = (first ? kSegFirst : 0) | ((gi == re - 1 || cur.j == cur.np - 1) ? kSegLast : 0) |
                      (cur.whole ? kPairWhole : 0);
           si.seg = cur.seg;
           si.nseg = cur.nseg;
@@ -509,9 +522,16 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
               tma_load_2d(vdst + nb * kBoxBytes, &vmap, nb * kBoxCols, y, fb);
             }
           }
-          // advance to the next page-head
-          if (++cur.j == cur.np && gi + 1 < r_end[rg]) locate(cur, gi + 1, pref, p, start, end, per, chunk);
-          if (gi + 1 < r_end[rg]) next_page = cur.trow[cur.first_page + cur.j];
+          // advance to the next page-head (and the table window with it)
+          if (++cur.j == cur.np && gi + 1 < re) {
+            locate(cur, gi + 1, pref, p, start, end, per, chunk);
+            window_entries(cur, e0, e1, e2, e3);
+          } else {
+            e0 = e1;
+            e1 = e2;
+            e2 = e3;
+            e3 = cur.np - cur.j > 3 ? cur.trow[cur.first_page + cur.j + 3] : 0;
+          }
         }
       }
       // the next chunk: claims are handed out in order, nchunks in all; the
@@ -990,12 +1010,15 @@ DecodeWorkspace decode_workspace_layout(int rows, int hkv, int group, int head_d
   return w;
 }
 
-cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch) {
+cudaError_t decode_prepare(int head_dim, bool kv8, int B, int hkv, DecodeLaunch* launch, bool fused) {
   // bf16 pools: two CTAs per SM (twice the warps, finer pieces) when there are
   // at least two (row, kv head) pairs per CTA of that grid, so that few pairs
   // are cut between CTAs; fewer pairs keep one CTA per SM and deeper rings.
+  // The one-kernel decode step takes two CTAs per SM as well: the next step's
+  // CTAs then fit beside this step's and run their prologue early.
   const int mode = kv8 ? kModeE4m3
-                       : (static_cast<long long>(B) * hkv >= 4ll * device_sm_count() ? kModeBf16Two : kModeBf16);
+                       : (fused || static_cast<long long>(B) * hkv >= 4ll * device_sm_count() ? kModeBf16Two
+                                                                                               : kModeBf16);
   switch (head_dim * 4 + mode) {
     case 256: return prepare_t<64, kModeBf16>(B, launch);
     case 257: return prepare_t<64, kModeBf16Two>(B, launch);
