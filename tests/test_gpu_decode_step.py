@@ -219,3 +219,38 @@ def test_decode_step_argument_errors_enqueue_nothing():
                                       w.B, dev.workspace, dev.ws_bytes, dev.status)
     torch.cuda.synchronize()
     assert np.array_equal(to_bits(dev.k_pool), k0)
+
+
+def test_decode_step_one_kernel_bad_data_is_flagged():
+    """Bad table data in the one-kernel form: the affected row skips its work
+    and a status bit is set; the other rows are unaffected and the context
+    stays healthy."""
+    import paged_kv_gqa_row_gb300 as lnk
+    grid = _grid()
+    rows = _rows_for(int(0.8 * grid), 8)
+    w = _case_workload("bad-data", 32, 8, 128, _lengths(rows, 70, 700, 17), 0, (), False)
+    assert _one_kernel(w, grid)
+    _, _, _, out_want = oracle_full(w)
+    # the page that holds row 1's new token: outside the pool
+    dev = DeviceStep(w, fill="host")
+    p1 = int(w.token_positions()[1])
+    dev.table[1, p1 // 64] = w.num_pages + 5
+    _decode_step(dev)
+    torch.cuda.synchronize()
+    assert int(dev.status.item()) & lnk.binding.DEV_BAD_PAGE
+    got = to_bits(dev.out)
+    assert np.all(np.isfinite(torch.from_numpy(got.view(np.int16)).view(torch.bfloat16).float().numpy()))
+    others = [b for b in range(w.B) if b != 1]
+    assert_attention_close(got[others], out_want[others], "rows with valid pages")
+    # a position past the table row: that row's output is zero
+    dev = DeviceStep(w, fill="host")
+    pos = dev.positions.clone()
+    pos[0] = w.pages_per_row * 64
+    dev.positions = pos
+    _decode_step(dev)
+    torch.cuda.synchronize()
+    assert int(dev.status.item()) & lnk.binding.DEV_BAD_POSITION
+    assert not np.any(to_bits(dev.out)[0])
+    assert_attention_close(to_bits(dev.out)[1:], out_want[1:], "rows after the bad one")
+    # the context is still healthy
+    _check_against_two_calls_and_oracle(w, 1)
