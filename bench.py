@@ -587,18 +587,19 @@ class GpuWorkload:
         ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot copied in
         ev_done = [torch.cuda.Event() for _ in range(2)]  # the slot's step finished (inputs read, output written)
         ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's output copied back
-        # Short steps are bound by the host's calls, not the copies: there the
-        # plain loop (copies and kernels in order on one stream) is faster.
-        pipelined = elapsed_ms > 0.05
+        # Short steps would be bound by the host's calls: there all the steps'
+        # copies and calls (the same streams and events) are captured once in a
+        # CUDA graph and replayed, as a serving loop of short steps would run
+        # them (the entry points allocate nothing and never synchronise).
+        use_graph = elapsed_ms <= 0.05
+        ev_fork = torch.cuda.Event()
+        ev_join = [torch.cuda.Event() for _ in range(2)]
 
-        def run(n):
-            if not pipelined:
-                with torch.cuda.stream(stream):
-                    for i in range(n):
-                        d_in[0].copy_(h_in, non_blocking=True)
-                        self.step(i, e_inputs[0], out_dst=d_out[0])
-                        h_out[0].copy_(d_out[0], non_blocking=True)
-                return
+        def run(n, fork_join=False):
+            if fork_join:  # bring the copy streams into the capture and back
+                ev_fork.record(stream)
+                up_stream.wait_event(ev_fork)
+                down_stream.wait_event(ev_fork)
             for i in range(n):
                 sl = i & 1
                 with torch.cuda.stream(up_stream):
@@ -616,24 +617,42 @@ class GpuWorkload:
                     down_stream.wait_event(ev_done[sl])
                     h_out[sl].copy_(d_out[sl], non_blocking=True)
                     ev_back[sl].record(down_stream)
+            if fork_join:
+                ev_join[0].record(up_stream)
+                ev_join[1].record(down_stream)
+                stream.wait_event(ev_join[0])
+                stream.wait_event(ev_join[1])
 
         run(3)
         torch.cuda.synchronize()
+        graph = None
+        if use_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                run(steps, fork_join=True)
+            graph.replay()
+            torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist:
             dist.barrier()
-        e0.record(up_stream if pipelined else stream)
-        run(steps)
-        e1.record(down_stream if pipelined else stream)
+        if graph is not None:
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            e1.record(stream)
+        else:
+            e0.record(up_stream)
+            run(steps)
+            e1.record(down_stream)
         torch.cuda.synchronize()
         self.check_status()
-        last = (steps - 1) & 1 if pipelined else 0
+        last = (steps - 1) & 1
         assert np.array_equal(h_out[last].numpy(), self.out.cpu().numpy()), \
             "end-to-end result differs from the device result"
         how = ("every step: inputs host->device and result device->host (pinned), each direction on its own "
-               "stream overlapping the kernels of the neighbouring steps (double buffers)" if pipelined else
-               "every step: inputs host->device, the kernels and the result device->host (pinned), in order "
-               "on one stream")
+               "stream overlapping the kernels of the neighbouring steps (double buffers)")
+        if use_graph:
+            how += "; all the steps' copies and calls captured once in a CUDA graph and replayed"
         return e0.elapsed_time(e1), h2d, d2h, how
 
 

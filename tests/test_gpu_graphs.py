@@ -90,3 +90,46 @@ def test_e4m3_decode_replays_equal_eager_calls():
         assert np.array_equal(to_bits(dev.out), want)
     assert int(dev.status.item()) == 0
     assert dev.desc.kv_dtype == lnk.KV_E4M3
+
+
+def test_one_kernel_decode_step_replays_equal_eager_calls():
+    """The one-kernel decode step (lnk_paged_decode_step on a small launch)
+    under capture: replays equal the eager call bit for bit, also after the
+    positions were moved on by one in place (read again by every replay)."""
+    w = synth.build("phi3_tiny")
+    dev = DeviceStep(w, fill="host")
+    assert dev.lnk.lnk_paged_decode_step_launches(dev.desc, w.B) == 1
+    k0, v0 = dev.k_pool.clone(), dev.v_pool.clone()
+    pos1 = dev.positions.clone()
+    pos2 = pos1 + 1  # still inside each row's last page or the next one of its table row
+    assert int(pos2.max().item()) < w.pages_per_row * 64
+
+    def call():
+        dev.lnk.lnk_paged_decode_step(dev.desc, dev.rope, dev.q, dev.k, dev.v, dev.positions, dev.table,
+                                      dev.gamma_q, dev.gamma_k, w.norm_eps, dev.k_pool, dev.v_pool, dev.q_out,
+                                      dev.out, w.B, dev.workspace, dev.ws_bytes, dev.status)
+
+    def eager(pos):
+        dev.k_pool.copy_(k0)
+        dev.v_pool.copy_(v0)
+        dev.positions.copy_(pos)
+        call()
+        torch.cuda.synchronize()
+        return to_bits(dev.out).copy(), to_bits(dev.k_pool).copy()
+
+    want1, kp1 = eager(pos1)
+    _, _, _, out_oracle = oracle_full(w)
+    assert_attention_close(want1, out_oracle, "phi3_tiny")
+    want2, kp2 = eager(pos2)
+    dev.positions.copy_(pos1)
+    graph = _graph_of(call)
+    for pos, want, kp in ((pos1, want1, kp1), (pos2, want2, kp2), (pos1, want1, kp1)):
+        dev.k_pool.copy_(k0)
+        dev.v_pool.copy_(v0)
+        dev.positions.copy_(pos)
+        dev.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(to_bits(dev.out), want)
+        assert np.array_equal(to_bits(dev.k_pool), kp)
+    assert int(dev.status.item()) == 0
