@@ -183,6 +183,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t0 = tile * TQ;
   const int nt = min(TQ, p.P - t0);
 
+  // ---- this CTA's query rows into shared memory (K-major, 128-byte swizzle:
+  // the A operand of Q.K^T), 16 bytes (eight head-dim columns) at a time, by
+  // the first softmax group right away, so that the loads overlap the tile's
+  // set-up (they are published on qfull after the cluster barrier) ----
+  if (warp >= 2 && warp < 6) {
+    const int rl = (warp & 3) * 32 + lane;
+    const int row = static_cast<int>(rank) * kRows + rl;  // token * G + head
+    const int tl = row / G, g = row % G;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 a = tl < nt ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + L::qsm + (c >> 3) * L::kQBox + swz128(rl, c & 7)) = a;
+    }
+    fence_proxy_async_smem();
+  }
+
   if (tid == 0) {
     // rank 0's full barriers also count the relay's arrival for rank 1's copy
     for (int s = 0; s < kStagesK; ++s) {
@@ -230,34 +248,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (bad && h == 0 && rank == 0 && p.status != nullptr) atomicOr(p.status, bad);
   }
   __syncthreads();
-  if (tid == 0) {
-    int nr = 0, cur = -1, steps = 0;
-    for (int i = 0; i < nt; ++i) {
-      if (tok_hi[i] <= tok_lo[i]) {
-        tok_run[i] = -1;
-        continue;
+  // ---- runs: maximal groups of the tile's valid tokens (in order, skipping
+  // tokens that see no key) with one table row; one warp, 32 tokens at a time ----
+  if (warp == 0) {
+    int nr = 0;           // runs so far
+    int last_row = 0;     // row of the last valid token so far
+    bool have_last = false;
+    for (int base = 0; base < TQ; base += 32) {
+      const int i = base + lane;
+      const bool v = i < nt && tok_hi[i] > tok_lo[i];
+      const int trow = tok_row[i];
+      const unsigned vm = __ballot_sync(0xffffffffu, v);
+      // row of the previous valid token: in this group of 32, else carried over
+      const unsigned before = vm & ((1u << lane) - 1u);
+      const int prev = __shfl_sync(0xffffffffu, trow, before ? 31 - __clz(before) : lane);
+      const bool has_prev = before != 0u || have_last;
+      const int prev_row = before ? prev : last_row;
+      const bool start = v && (!has_prev || prev_row != trow);
+      const unsigned sm = __ballot_sync(0xffffffffu, start);
+      const int rid = nr + __popc(sm & ((2u << lane) - 1u)) - 1;  // (lane 31: all bits)
+      tok_run[i] = v ? rid : -1;
+      if (start) {
+        run_row[rid] = trow;
+        run_kmin[rid] = tok_lo[i];
+        run_kmax[rid] = tok_hi[i];
       }
-      const int row = tok_row[i];
-      if (cur < 0 || run_row[cur] != row) {
-        cur = nr++;
-        run_row[cur] = row;
-        run_kmin[cur] = tok_lo[i];
-        run_kmax[cur] = tok_hi[i];
-      } else {
-        run_kmin[cur] = min(run_kmin[cur], tok_lo[i]);
-        run_kmax[cur] = max(run_kmax[cur], tok_hi[i]);
+      __syncwarp();
+      if (v && !start) {
+        atomicMin(run_kmin + rid, tok_lo[i]);
+        atomicMax(run_kmax + rid, tok_hi[i]);
       }
-      tok_run[i] = cur;
+      __syncwarp();
+      nr += __popc(sm);
+      if (vm) {
+        last_row = __shfl_sync(0xffffffffu, trow, 31 - __clz(vm));
+        have_last = true;
+      }
     }
-    for (int i = nt; i < TQ; ++i) tok_run[i] = -1;
-    for (int r = 0; r < nr; ++r) {
+    int steps = 0;
+    for (int r = lane; r < nr; r += 32) {
       run_first[r] = run_kmin[r] / kPage;
       const int pages = (run_kmax[r] - 1) / kPage - run_first[r] + 1;
       run_steps[r] = (pages + 1) / 2;
       steps += run_steps[r];
     }
-    misc[0] = nr;
-    misc[1] = steps;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) steps += __shfl_xor_sync(0xffffffffu, steps, o);
+    if (lane == 0) {
+      misc[0] = nr;
+      misc[1] = steps;
+    }
   }
   // barriers initialised and tensor memory allocated in both CTAs before any
   // thread of either uses them
@@ -422,18 +462,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int* fin_ok = reinterpret_cast<int*>(fin_l + 2 * kRows);
     const size_t qrow = (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
     const uint32_t pfull0 = mapa_shared(smem_addr(pfull), 0);
-    // ---- this row's query into shared memory (K-major, 128-byte swizzle: the
-    // A operand of Q.K^T), 16 bytes (eight head-dim columns) at a time ----
+    // this group's query rows are in shared memory (written before the
+    // cluster barrier); the peer's tensor core reads them too: publish at
+    // cluster scope
     if (nsteps > 0 && grp == 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 a = tl < nt ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + L::qsm + (c >> 3) * L::kQBox + swz128(rl, c & 7)) = a;
-      }
-      fence_proxy_async_smem();
       __syncwarp();
-      // (the peer's tensor core reads these rows: publish at cluster scope)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(qfull), 0));
     }
     // Every wait's outcome is made warp-uniform: the tensor-memory loads and
