@@ -72,8 +72,8 @@ struct TcSmem {
   static constexpr size_t vring = kring + size_t(kStagesK) * kKStage;
   static constexpr size_t qsm = vring + size_t(kStagesV) * kVStage;  // this CTA's query rows, K-major
   static constexpr size_t bars = qsm + size_t(NB) * kQBox;
-  // kfull[K], kempty[K], vfull[V], vempty[V], sfull[2], sfree[2], pfull[2], pvdone[2], odone, qfull
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 10;
+  // kfull[K], kempty[K], vfull[V], vempty[V], sfull[2], sfree[2], pfull[2], pvdone[2], odone
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 9;
   static constexpr size_t tok = bars + kNumBars * sizeof(uint64_t);
   static constexpr size_t runs = tok + 4 * kTileRows * 4;
   static constexpr size_t misc = runs + 5 * kTileRows * 4;  // [0] runs, [1] steps, [2] abort, [3] tmem, [4] tile
@@ -131,7 +131,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* pfull = sfree + 2;           // [2] P_b written (rank 0 only)
   uint64_t* pvdone = pfull + 2;          // [2] P.V from P_b finished (all but the last)
   uint64_t* odone = pvdone + 2;          // the last P.V
-  uint64_t* qfull = odone + 1;           // rank 0 only
   int* tok_lo = reinterpret_cast<int*>(smem + L::tok);
   int* tok_hi = tok_lo + kTileRows;
   int* tok_run = tok_hi + kTileRows;
@@ -184,20 +183,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nt = min(TQ, p.P - t0);
 
   // ---- this CTA's query rows into shared memory (K-major, 128-byte swizzle:
-  // the A operand of Q.K^T), 16 bytes (eight head-dim columns) at a time, by
-  // the first softmax group right away, so that the loads overlap the tile's
-  // set-up (they are published on qfull after the cluster barrier) ----
+  // the A operand of Q.K^T), by the first softmax group right away, so that
+  // the loads overlap the tile's set-up: all of a row's 16-byte pieces are
+  // loaded before any is stored.  The cluster barrier below publishes them to
+  // the pair's tensor cores (each thread orders its stores before the async
+  // proxy first). ----
   if (warp >= 2 && warp < 6) {
     const int rl = (warp & 3) * 32 + lane;
     const int row = static_cast<int>(rank) * kRows + rl;  // token * G + head
     const int tl = row / G, g = row % G;
     const uint4* src = reinterpret_cast<const uint4*>(
         p.q + (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D);
+    uint4 a[D / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 a = tl < nt ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(smem + L::qsm + (c >> 3) * L::kQBox + swz128(rl, c & 7)) = a;
-    }
+    for (int c = 0; c < D / 8; ++c) a[c] = tl < nt ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      *reinterpret_cast<uint4*>(smem + L::qsm + (c >> 3) * L::kQBox + swz128(rl, c & 7)) = a[c];
     fence_proxy_async_smem();
   }
 
@@ -218,7 +220,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(pvdone + b), 1);
     }
     mbar_init(smem_addr(odone), 1);
-    mbar_init(smem_addr(qfull), 8);
     misc[2] = 0;
     fence_mbarrier_init();
   }
@@ -387,8 +388,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t qdesc0 = umma_desc_sw128(smem_addr(smem + L::qsm), 0, 1024);
       // S_b = Q K^T of step j, once the softmax has read S_b of step j - 2
       // (sfree is at most one phase past that: the softmax reads S_b of step
-      // j only after this product) and both CTAs' K pages have landed.
-      bool ok = mbar_wait(smem_addr(qfull), 0, abort_flag);
+      // j only after this product) and both CTAs' K pages have landed.  (Both
+      // CTAs' query rows were stored before the cluster barrier.)
+      bool ok = true;
       for (int j = 0; ok && j < nsteps; ++j) {
         const int b = j & 1, sk = j % kStagesK;
         ok = (j < 2 || mbar_wait(smem_addr(sfree + b), ((j - 2) >> 1) & 1, abort_flag)) &&
@@ -462,13 +464,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int* fin_ok = reinterpret_cast<int*>(fin_l + 2 * kRows);
     const size_t qrow = (static_cast<size_t>(t0 + tl) * p.hq + static_cast<size_t>(h) * G + g) * D;
     const uint32_t pfull0 = mapa_shared(smem_addr(pfull), 0);
-    // this group's query rows are in shared memory (written before the
-    // cluster barrier); the peer's tensor core reads them too: publish at
-    // cluster scope
-    if (nsteps > 0 && grp == 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(qfull), 0));
-    }
     // Every wait's outcome is made warp-uniform: the tensor-memory loads and
     // stores that follow are warp-collective.
     float m_ref = -INFINITY;   // the row's running max (log2 units) after this group's last step
@@ -664,28 +659,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float lb = mo == -INFINITY ? 0.f : lo_ * exp2f(mo - mf);
       l_part = grp == 0 ? la + lb : lb + la;
     }
+    // this group's half of the row: all of its columns read from tensor
+    // memory at once, then stored 16 bytes at a time
     uint16_t* dst = p.out + qrow + grp * (D / 2);
     const float inv = l_part > 0.f ? 1.f / l_part : 0.f;
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t r[16];
-      if (ok && nsteps > 0) {
-        tmem_ld16(tmem + lanes + L::kColO + grp * (D / 2) + c * 16, r);
-        tmem_ld_wait();
-      } else {
+    uint32_t r[D / 2];
+    if (ok && nsteps > 0) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t (&rc)[16] = *reinterpret_cast<uint32_t(*)[16]>(r + c * 16);
+        tmem_ld16(tmem + lanes + L::kColO + grp * (D / 2) + c * 16, rc);
       }
-      if (tl < nt) {
-        uint2* o = reinterpret_cast<uint2*>(dst + c * 16);
+      tmem_ld_wait();
+    } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a0v = live ? __uint_as_float(r[4 * i]) * inv : 0.f;
-          const float a1v = live ? __uint_as_float(r[4 * i + 1]) * inv : 0.f;
-          const float a2v = live ? __uint_as_float(r[4 * i + 2]) * inv : 0.f;
-          const float a3v = live ? __uint_as_float(r[4 * i + 3]) * inv : 0.f;
-          o[i] = make_uint2(pack_bf16x2(a0v, a1v), pack_bf16x2(a2v, a3v));
-        }
+      for (int i = 0; i < D / 2; ++i) r[i] = 0u;
+    }
+    if (tl < nt) {
+      uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = live ? __uint_as_float(r[8 * i + k]) * inv : 0.f;
+        o[i] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                          pack_bf16x2(v[6], v[7]));
       }
     }
   }
