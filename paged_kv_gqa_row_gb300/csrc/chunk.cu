@@ -10,33 +10,35 @@
 // rows; the pages covering each run's key range are streamed once, two pages
 // (128 keys) per step, for all 256 rows.
 //
-// Products are 2-SM (M = 256) and issued by one thread of rank 0:
-//   S_b[256 x 128] = Q K_j^T   Q from each CTA's tensor memory (bf16 pairs),
-//                              K_j K-major in shared memory: rank r holds page
-//                              2j + r of the step (keys 64 r .. 64 r + 63);
-//   O[256 x 128]  += P_b V_j   P from tensor memory (bf16, written over the
-//                              first 64 columns of S_b), V_j MN-major: rank r
-//                              holds head-dim columns 64 r .. 64 r + 63 of both
-//                              pages.
-// S is double-buffered (b = j mod 2), so Q K^T of step j + 1 runs on the
-// tensor cores while the softmax works on step j.  Products issued by one
-// thread run in order: Q K^T of step j + 2 overwrites S_b only after P V of
-// step j has read P from it.
+// Products are 2-SM (M = 256), issued by two threads of rank 0:
+//   S_b[256 x 128] = Q K_j^T   Q K-major in each CTA's shared memory (its 128
+//                              rows), K_j K-major in shared memory: rank r
+//                              holds page 2j + r of the step (keys
+//                              64 r .. 64 r + 63);
+//   O[256 x 128]  += P_b V_j   P_b from tensor memory (bf16 pairs), V_j
+//                              MN-major: rank r holds head-dim columns
+//                              64 r .. 64 r + 63 of both pages.
+// S and P are double-buffered (b = j mod 2), so Q K^T of step j + 1 runs on
+// the tensor cores while the softmax works on step j.
 //
-// CTA structure (192 threads, warp-specialised, both ranks):
+// CTA structure (352 threads, warp-specialised, both ranks):
 //  * warp 0, producer: TMA loads of this CTA's K page and V columns into
-//    rings of stages;
-//  * warp 1: in rank 0, the MMA thread; in rank 1, a relay that tells rank 0
-//    when rank 1's stages have landed (rank 0's MMA reads both CTAs' stages);
-//  * warps 2-5, softmax: thread r owns query row r of its CTA (tensor-memory
-//    lane r).  It writes its query row into tensor memory; then, per step,
-//    reads 128 scores, masks them (same run, lo <= key <= position, valid
-//    page), updates the running max and sum in registers, writes P, and
-//    rescales its row of O only when the running max grows by more than 2^8
-//    (until then P stays below 256, exact enough in bf16); at the end it
-//    normalises its row of O and stores it.
-// Barriers that the other CTA arrives on live in rank 0 (the Q, P and
-// relay barriers); the 2-SM commits arrive in both CTAs at once.
+//    rings of stages (and, before that, the tile's runs of tokens);
+//  * warp 1: in rank 0, the Q.K^T issuer; in rank 1, a relay that tells rank
+//    0 when rank 1's stages have landed (rank 0's products read both CTAs'
+//    stages);
+//  * warp 10: in rank 0, the P.V issuer;
+//  * warps 2-9, softmax, in two groups of four warps taking alternate steps:
+//    thread r of a group owns query row r of its CTA (tensor-memory lane r).
+//    The first group loads the CTA's query rows into shared memory at the
+//    start.  Per step, a group reads 128 scores, masks them (same run,
+//    lo <= key <= position, valid page), updates the running max (handed on
+//    to the other group) and its partial sum, writes P, and rescales its row
+//    of O only when the running max grows by more than 2^8 (until then P stays
+//    below 256, exact enough in bf16); at the end the groups combine their
+//    sums and each normalises and stores half of the row of O.
+// Barriers that the other CTA arrives on live in rank 0 (the P and relay
+// barriers); the 2-SM commits arrive in both CTAs at once.
 //
 // Sources: "Mistral 7B Instruct v0.3", Entries table (prefill_paged: prompts
 // packed end to end, each token written at its place in the pool and attending
