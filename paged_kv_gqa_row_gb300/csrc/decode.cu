@@ -347,13 +347,21 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     plan_chunk(blockIdx.x, first_plan);
 
   // Wait for the previous kernel on the stream (it writes q and the pool).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The producer warp waits later, right before its first copy: the first
+  // stage's bookkeeping then runs before the wait, which also brings the
+  // producer's code into the instruction cache (run first after the wait, it
+  // took about 1200 cycles to reach the first copy).
+  if (warp != kProducerWarp) asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // rows with nothing to attend to get a zero output
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
-    if (pref[b + 1] == pref[b]) {
-      uint32_t* o = reinterpret_cast<uint32_t*>(p.out + static_cast<size_t>(b) * p.hq * D);
-      for (int i = tid; i < p.hq * D / 2; i += kThreads) o[i] = 0u;
+  // rows with nothing to attend to get a zero output (the producer warp does
+  // not take part: it has not waited yet)
+  if (warp != kProducerWarp) {
+    const int zt = warp < kProducerWarp ? tid : tid - 32;
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+      if (pref[b + 1] == pref[b]) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(p.out + static_cast<size_t>(b) * p.hq * D);
+        for (int i = zt; i < p.hq * D / 2; i += kThreads - 32) o[i] = 0u;
+      }
     }
   }
   if (static_cast<long long>(blockIdx.x) >= nchunks) return;
@@ -459,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
     // (fused step: the consumers write the rotated queries themselves)
     const uint32_t q_bytes = fused ? 0u : static_cast<uint32_t>(G * D * 2);
     int k = 0;
-    bool stop = false;
+    bool stop = false, waited = false;
     Cursor cur;
     for (long long chunk = blockIdx.x; chunk < nchunks && !stop;) {
       ChunkPlan pl;
@@ -508,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
           const uint32_t fb = smem_addr(full_bar + s);
           const uint32_t tx = (valid ? static_cast<uint32_t>(L::kStageBytes) : 0u) + (first ? q_bytes : 0u);
           if (tx) mbar_arrive_expect_tx(fb, tx); else mbar_arrive(fb);
+          if (!waited) {  // (the previous kernel writes q and the pool)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
+          }
           if (first && q_bytes > 0) {
             const uint16_t* qsrc = p.q + (static_cast<size_t>(cur.b) * p.hq + static_cast<size_t>(cur.h) * G) * D;
             bulk_load(smem_addr(smem + L::qbuf + size_t(s) * L::kQBytes), qsrc, q_bytes, fb);
