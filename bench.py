@@ -53,6 +53,9 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1700.0
 
 
+L2_FALLBACK = 129 * 1024 * 1024  # GB300 L2, when the device does not report it
+
+
 def algorithmic_bytes(w, kv_bytes: int = 2) -> dict:
     """Bytes a step must move at least once, by part (kv_bytes: bytes per pool
     element, 2 for bf16 pools, 1 for 8-bit pools)."""
@@ -351,7 +354,19 @@ class GpuWorkload:
         self.kv_bytes = 1 if e4m3 else 2
         self.parts = algorithmic_bytes(w, self.kv_bytes)
         self.pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * self.kv_bytes
-        self.copies = args.pool_copies or (2 if self.pool_bytes < (8 << 30) else 1)
+        # Pool copies alternated step to step, so that a copy comes back only
+        # after the steps in between have read more than twice the L2 (a
+        # small workload's pages would otherwise stay in L2 from one step to
+        # the next); pools of 8 GB and more are read whole each step (one copy).
+        self.l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_FALLBACK)
+        self.read_per_step = max(1, self.parts["decode_kv"] + self.parts["chunk_kv"])
+        if args.pool_copies:
+            self.copies = args.pool_copies
+        elif self.pool_bytes >= (8 << 30):
+            self.copies = 1
+        else:
+            need = 1 + -(-2 * self.l2_bytes // self.read_per_step)
+            self.copies = max(2, min(need, (8 << 30) // self.pool_bytes))
 
         def d16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
@@ -391,6 +406,16 @@ class GpuWorkload:
         else:
             self.launches_per_step = 1 + 1 + (1 if w.B else 0)
         self.one_kernel = w.P == 0 and self.launches_per_step == 1
+
+    def l2_note(self):
+        """How the timed steps keep their K/V reads out of L2."""
+        between = (self.copies - 1) * self.read_per_step
+        if self.copies == 1:
+            return (f"inputs larger than L2: one pool of {self.pool_bytes / 1e9:.2f} GB, "
+                    f"{self.read_per_step / 1e9:.2f} GB of K/V read per step (L2 {self.l2_bytes / 1e6:.0f} MB)")
+        return (f"inputs larger than L2: {self.copies} pool copies of {self.pool_bytes / 1e9:.3f} GB alternated "
+                f"step to step; a copy comes back after {between / 1e6:.0f} MB of other steps' K/V reads "
+                f"(L2 {self.l2_bytes / 1e6:.0f} MB)")
 
     def attend(self, kp, vp, q_src, out_dst, tab):
         w, lnk = self.w, self.lnk
@@ -711,8 +736,7 @@ def run_gpu(args, rank, world, dist):
                  "ms_per_step": round(m_ms / args.steps, 5),
                  "row_steps_per_s": round(world * wm.B * args.steps / (m_ms / 1e3), 1),
                  "algorithmic_bytes_per_step": m_step,
-                 "l2": f"inputs larger than L2: {gm.copies} pool copies of {gm.pool_bytes / 1e9:.2f} GB, "
-                       "alternated step to step",
+                 "l2": gm.l2_note(),
                  "roofline": gm.roofline(m_times, "mistral", kt_steps)}
         del gm
 
@@ -731,8 +755,7 @@ def run_gpu(args, rank, world, dist):
                    "scale": args.scale, "decode_rows": w.B, "chunk_tokens": w.P, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.head_dim, "page_size": 64, "num_pages": w.num_pages,
                    "parallelism": f"rows x{world} (independent batches per GPU)",
-                   "l2": f"inputs larger than L2: {g.copies} pool copies of {g.pool_bytes / 1e9:.2f} GB, "
-                         "alternated step to step",
+                   "l2": g.l2_note(),
                    "algorithmic_bytes_per_step": step_bytes},
         "row_steps_per_s": round(world * w.B * args.steps / (elapsed_ms / 1e3), 1),
         "chunk_tokens_per_s": round(world * w.P * args.steps / (elapsed_ms / 1e3), 1),
