@@ -343,8 +343,28 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   // previous kernel on the stream).
   ChunkPlan first_plan;
   first_plan.nranges = 0;
-  if (warp == kProducerWarp && lane == 0 && static_cast<long long>(blockIdx.x) < nchunks)
+  if (warp == kProducerWarp && lane == 0 && static_cast<long long>(blockIdx.x) < nchunks) {
     plan_chunk(blockIdx.x, first_plan);
+    // One short pair per CTA: through a short ring its pages would take a
+    // DRAM round trip per ring's worth, so all of them are prefetched into L2
+    // first.  (Prefetches only: whatever the previous kernel writes to these
+    // pages still reaches L2 before this kernel's copies read them, after the
+    // wait.)
+    if (pair_chunks && first_plan.nranges > 0) {
+      const Cursor& c = first_plan.cur;
+      for (int j = c.j; j < c.np; ++j) {
+        const int page = c.trow[c.first_page + j];
+        if (page >= 0 && page < p.num_pages) {
+          const int y = (c.h * p.num_pages + page) * kPage;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            tma_prefetch_l2_2d(&kmap, nb * kBoxCols, y);
+            tma_prefetch_l2_2d(&vmap, nb * kBoxCols, y);
+          }
+        }
+      }
+    }
+  }
 
   // Wait for the previous kernel on the stream (it writes q and the pool).
   // The producer warp waits later, right before its first copy: the first

@@ -105,6 +105,14 @@ __device__ __forceinline__ void tma_prefetch_descriptor(const CUtensorMap* map) 
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Prefetch of a 2-D tile into L2 (no shared memory, no barrier).  x follows
+// the same 16-byte rule as the loads.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tiled bulk copy global -> shared, completing on `bar` (complete_tx).
 // x (innermost coordinate, elements) must be a multiple of 8 for 16-bit data.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
