@@ -215,7 +215,11 @@ lnk_status lnk_paged_append_rope(const lnk_attn_desc* desc, const lnk_rope_desc*
  * Ordering with the preceding kernel: the decode kernel is launched as a
  * programmatic dependent launch and reads `positions` and `table` (and only
  * those) before it waits for the kernel before it on the stream; q, the pools
- * and the workspace are touched after the wait.  So `positions` and `table`
+ * and the workspace are touched after the wait.  (When every (row, kv head)
+ * pair is one CTA's whole work, the kernel also asks L2 to prefetch the pair's
+ * pool pages before the wait: a prefetch reads no values into the kernel, and
+ * what the preceding kernel writes to those pages is what the kernel's copies
+ * read after the wait.)  So `positions` and `table`
  * must not be written by the kernel immediately preceding this call on the
  * same stream (lnk_paged_append_rope only reads them); a caller that computes
  * them on the device should write them earlier, or put another operation in
