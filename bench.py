@@ -54,6 +54,19 @@ FALLBACK_BF16_TFLOPS = 1700.0
 
 
 L2_FALLBACK = 129 * 1024 * 1024  # GB300 L2, when the device does not report it
+POOL_COPY_LIMIT = 8 << 30         # pools of this size and more are read whole each step (one copy)
+
+
+def pool_copies(pool_bytes: int, read_per_step: int, l2_bytes: int, requested: int = 0) -> int:
+    """Pool copies alternated step to step, so that a copy comes back only after
+    the steps in between have read more than twice the L2 (at most
+    POOL_COPY_LIMIT of pools in all)."""
+    if requested:
+        return requested
+    if pool_bytes >= POOL_COPY_LIMIT:
+        return 1
+    need = 1 + -(-2 * l2_bytes // max(1, read_per_step))
+    return max(2, min(need, POOL_COPY_LIMIT // pool_bytes))
 
 
 def algorithmic_bytes(w, kv_bytes: int = 2) -> dict:
@@ -354,19 +367,10 @@ class GpuWorkload:
         self.kv_bytes = 1 if e4m3 else 2
         self.parts = algorithmic_bytes(w, self.kv_bytes)
         self.pool_bytes = 2 * w.hkv * w.pool_positions * w.head_dim * self.kv_bytes
-        # Pool copies alternated step to step, so that a copy comes back only
-        # after the steps in between have read more than twice the L2 (a
-        # small workload's pages would otherwise stay in L2 from one step to
-        # the next); pools of 8 GB and more are read whole each step (one copy).
+        # (a small workload's pages would otherwise stay in L2 from one step to the next)
         self.l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_FALLBACK)
         self.read_per_step = max(1, self.parts["decode_kv"] + self.parts["chunk_kv"])
-        if args.pool_copies:
-            self.copies = args.pool_copies
-        elif self.pool_bytes >= (8 << 30):
-            self.copies = 1
-        else:
-            need = 1 + -(-2 * self.l2_bytes // self.read_per_step)
-            self.copies = max(2, min(need, (8 << 30) // self.pool_bytes))
+        self.copies = pool_copies(self.pool_bytes, self.read_per_step, self.l2_bytes, args.pool_copies)
 
         def d16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)

@@ -102,3 +102,29 @@ def test_reference_arm_prints_one_json_line(config):
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert np.isfinite(d["ms_per_step"]) and d["ms_per_step"] > 0
+
+
+@pytest.mark.parametrize("name", ["phi3_tiny", "mistral", "phi3_window", "qwen3", "llama_prefill"])
+@pytest.mark.parametrize("kv_bytes", [2, 1])
+def test_pool_copies_keep_reads_out_of_l2(name, kv_bytes):
+    """The timed steps alternate pool copies so that a copy's pages were evicted
+    before it comes back: the other copies' reads in between exceed twice the L2."""
+    if kv_bytes == 1 and name == "llama_prefill":
+        pytest.skip("chunk attention runs on bf16 pools only")
+    w = synth.build(name)
+    parts = bench.algorithmic_bytes(w, kv_bytes)
+    pool = 2 * w.hkv * w.pool_positions * w.head_dim * kv_bytes
+    read = parts["decode_kv"] + parts["chunk_kv"]
+    for l2 in (bench.L2_FALLBACK, 136 * 10**6):
+        c = bench.pool_copies(pool, read, l2)
+        assert c >= 2 and c * pool <= max(bench.POOL_COPY_LIMIT, 2 * pool)
+        assert (c - 1) * read > 2 * l2
+    assert bench.pool_copies(pool, read, bench.L2_FALLBACK, requested=3) == 3
+
+
+def test_pool_copies_large_pool_is_read_whole():
+    w = synth.build("llama_step", scale=1.0)
+    pool = 2 * w.hkv * w.pool_positions * w.head_dim * 2
+    read = bench.algorithmic_bytes(w)["decode_kv"]
+    assert pool >= bench.POOL_COPY_LIMIT and read > 2 * bench.L2_FALLBACK
+    assert bench.pool_copies(pool, read, bench.L2_FALLBACK) == 1
