@@ -56,8 +56,11 @@
 // The per-row prologue (visible pages, prefix sums, the producer's plan of its
 // first chunk) reads only positions and the table, so it overlaps the
 // previous kernel on the stream (programmatic dependent launch); the kernel
-// waits for that kernel before touching q or the pool.  It lets the next
-// kernel on the stream start early in the same way.
+// waits for that kernel before touching q or the pool.  The producer warp
+// waits last, right before its first copy, once its first stage's record is
+// written; with one short pair per CTA it also asks L2 to prefetch the pair's
+// pages before the wait (a prefetch reads nothing into the kernel).  The
+// kernel lets the next kernel on the stream start early in the same way.
 //
 // Sources: "Phi-3 Mini 4K Instruct -- files", src/attention.linnet
 // (decode_rows: a row attends over itself up to its position; window_mask;
@@ -260,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, MODE == kModeBf16 ? 1 : 2)
   // Several chunks per CTA only when pairs are many (and so short) against a
   // CTA's share: each chunk boundary cuts a pair, and a cut pair costs a
   // partial result and a merge.
-  // (8-bit pools: the consumers, not the memory, set the pace; one chunk.)
+  // (8-bit pools keep one chunk per CTA: there, finer chunks measured slower,
+  // their cut pairs' partials and merges costing more than the balance gained.)
   const int chunks_per_cta = !F8 && static_cast<long long>(B) * p.hkv >= 5ll * gridDim.x ? kChunksPerCta : 1;
   const long long per = (total + chunks_per_cta * gridDim.x - 1) / (chunks_per_cta * gridDim.x);  // chunk size
   const long long nchunks = pair_chunks ? pairs : (per > 0 ? (total + per - 1) / per : 0);
